@@ -1,0 +1,89 @@
+"""ctypes loader and raw signatures of libcp (include/cp.h).
+
+The library must exist: there is no fallback path.  Build it with
+``python -m context_parallelism_02_gb300.build`` (or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+CP_OK = 0
+CP_EINVAL = -1
+CP_EHEADS = -2
+CP_EUNSUPPORTED = -3
+CP_ECUDA = -4
+CP_ETIMEOUT = -5
+
+CP_LAYOUT_CONTIGUOUS = 0
+CP_LAYOUT_ZIGZAG = 1
+CP_F32 = 0
+CP_BF16 = 1
+
+# name -> (restype, argtypes); mirrors include/cp.h
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_F = ctypes.c_float
+SIGNATURES = {
+    "cp_shard_map": (_I, [_L, _I, _I, _P]),
+    "cp_schedule_pairs": (_I, [_L, _I, _I, _I, _P, _P]),
+    "ring_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _P]),
+    "ring_attn_fwd_rank": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _I,
+                                _I, _P]),
+    "lse_merge": (_I, [_P, _P, _P, _P, _P, _P, _L, _I, _P]),
+    "ulysses_seq_to_head": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),
+    "ulysses_head_to_seq": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),
+    "cp_get_error": (_I, [_P]),
+    "cp_strerror": (ctypes.c_char_p, [_I]),
+    "cp_debug_wait_timeout": (_I, [ctypes.c_uint64, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CpError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (code {code})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libcp.so (raises if it is missing: no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise RuntimeError(
+                        f"libcp.so not found at {path}; build it with "
+                        "`python -m context_parallelism_02_gb300.build`")
+                _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().cp_strerror(code).decode()
+    except Exception:  # noqa: BLE001 - message lookup must not mask the real error
+        return f"status {code}"
+
+
+def check(code: int, what: str):
+    if code != CP_OK:
+        raise CpError(code, what)

@@ -1,0 +1,149 @@
+"""Python binding of libcp: same names as the C ABI, argument marshalling only.
+
+Tensors are torch tensors on the current CUDA device (torch supplies device
+memory and streams); every computation runs in libcp's CUDA kernels.  Outputs
+are allocated with torch when not given.  Each call is asynchronous on the
+current torch stream (or ``stream``), like the C call.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import CP_BF16, CP_F32, CpError, check  # noqa: F401
+
+_DT = {torch.float32: CP_F32, torch.bfloat16: CP_BF16}
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda_contig(name, t):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def cp_shard_map(S: int, N: int, layout: int) -> np.ndarray:
+    """Global position of each local row, int32 ``[N, S/N]`` (host)."""
+    out = np.zeros(S, dtype=np.int32)
+    check(_lib.load().cp_shard_map(S, N, layout, out.ctypes.data_as(ctypes.c_void_p)),
+          "cp_shard_map")
+    return out.reshape(N, S // N)
+
+
+def cp_schedule_pairs(S: int, N: int, layout: int, causal: bool):
+    """(masked-in pairs, executed 128x128 tile pairs) per (rank, step), int64 ``[N, N]``."""
+    pairs = np.zeros(N * N, dtype=np.int64)
+    tiles = np.zeros(N * N, dtype=np.int64)
+    check(_lib.load().cp_schedule_pairs(S, N, layout, int(causal),
+                                        pairs.ctypes.data_as(ctypes.c_void_p),
+                                        tiles.ctypes.data_as(ctypes.c_void_p)),
+          "cp_schedule_pairs")
+    return pairs.reshape(N, N), tiles.reshape(N, N)
+
+
+def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, N: int, layout: int,
+                  causal: bool = True, scale: float | None = None, out=None, lse=None,
+                  stream=None, rank_range: tuple[int, int] | None = None):
+    """Ring / context-parallel attention forward; returns (out, lse).
+
+    q ``[B,S,Hq,D]``, k/v ``[B,S,Hkv,D]`` (fp32 or bf16, global order);
+    out like q, lse ``[B,Hq,S]`` fp32.  ``rank_range=(lo, hi)`` restricts the
+    computed queries to virtual ranks [lo, hi) (``ring_attn_fwd_rank``).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(name, t)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share dtype float32 or bfloat16")
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _need_cuda_contig("out", out)
+    _need_cuda_contig("lse", lse)
+    sc = -1.0 if scale is None else float(scale)
+    L = _lib.load()
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, N, int(causal),
+            layout, _DT[q.dtype], sc)
+    if rank_range is None:
+        rc = L.ring_attn_fwd(*args, ctypes.c_void_p(_stream(stream)))
+        check(rc, "ring_attn_fwd")
+    else:
+        rc = L.ring_attn_fwd_rank(*args, rank_range[0], rank_range[1],
+                                  ctypes.c_void_p(_stream(stream)))
+        check(rc, "ring_attn_fwd_rank")
+    return out, lse
+
+
+def lse_merge(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
+    """Merge two fp32 partials over disjoint key sets; returns (out, lse)."""
+    for name, t in (("out_a", out_a), ("lse_a", lse_a), ("out_b", out_b), ("lse_b", lse_b)):
+        _need_cuda_contig(name, t)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    rows = lse_a.numel()
+    D = out_a.numel() // max(rows, 1)
+    if out is None:
+        out = torch.empty_like(out_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    rc = _lib.load().lse_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
+                               _ptr(lse), rows, D, ctypes.c_void_p(_stream(stream)))
+    check(rc, "lse_merge")
+    return out, lse
+
+
+def ulysses_seq_to_head(x: torch.Tensor, N: int, layout: int, y=None, stream=None):
+    """``[N, B, S/N, H, D]`` rank-major shards -> ``[N, B, S, H/N, D]`` head groups."""
+    _need_cuda_contig("x", x)
+    Nn, B, Lr, H, D = x.shape
+    if Nn != N:
+        raise ValueError("x.shape[0] must equal N")
+    if y is None:
+        y = torch.empty((N, B, N * Lr, H // N if H % N == 0 else 1, D), dtype=x.dtype,
+                        device=x.device)
+    rc = _lib.load().ulysses_seq_to_head(_ptr(x), _ptr(y), B, N * Lr, H, D, N, layout,
+                                         x.element_size(), ctypes.c_void_p(_stream(stream)))
+    check(rc, "ulysses_seq_to_head")
+    return y
+
+
+def ulysses_head_to_seq(y: torch.Tensor, N: int, layout: int, x=None, stream=None):
+    """Inverse of :func:`ulysses_seq_to_head`."""
+    _need_cuda_contig("y", y)
+    Nn, B, S, hg, D = y.shape
+    if Nn != N:
+        raise ValueError("y.shape[0] must equal N")
+    if x is None:
+        x = torch.empty((N, B, S // N, hg * N, D), dtype=y.dtype, device=y.device)
+    rc = _lib.load().ulysses_head_to_seq(_ptr(y), _ptr(x), B, S, hg * N, D, N, layout,
+                                         y.element_size(), ctypes.c_void_p(_stream(stream)))
+    check(rc, "ulysses_head_to_seq")
+    return x
+
+
+def cp_get_error(stream=None) -> int:
+    """Synchronise the stream and read+clear the device error word (a status code)."""
+    return _lib.load().cp_get_error(ctypes.c_void_p(_stream(stream)))
+
+
+def cp_strerror(code: int) -> str:
+    return _lib.strerror(code)
+
+
+def cp_debug_wait_timeout(limit_ns: int, stream=None):
+    check(_lib.load().cp_debug_wait_timeout(limit_ns, ctypes.c_void_p(_stream(stream))),
+          "cp_debug_wait_timeout")

@@ -1,0 +1,263 @@
+// cp_api.cu -- the extern "C" entry points of libcp (declared in cp.h):
+// argument checking, dispatch to the kernels, and the per-device error word.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "cp.h"
+#include "cp_common.cuh"
+#include "kernels.h"
+
+namespace cp {
+
+// Per-device error word: a kernel whose bounded wait runs out writes a code
+// here (first writer wins); cp_get_error reads and clears it.
+__device__ unsigned g_err_word;
+
+namespace {
+
+constexpr int MAX_DEV = 64;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s per device-side wait
+
+unsigned *err_ptr()
+{
+    static unsigned *ptrs[MAX_DEV] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned *>(p);
+    }
+    return ptrs[dev];
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_shard(int64_t S, int N, int layout)
+{
+    if (N < 1 || S < 0 || S > 0x7fffffffLL) return CP_EINVAL;
+    if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_ZIGZAG) return CP_EINVAL;
+    if (S % N) return CP_EINVAL;
+    if (layout == CP_LAYOUT_ZIGZAG && S % (2 * (int64_t)N)) return CP_EINVAL;
+    return CP_OK;
+}
+
+// sum over queries i in [qa, qb) of |{j in [ks, ks+L) : j <= i}|, in closed form
+int64_t visible_pairs(int64_t qa, int64_t qb, int64_t ks, int64_t L)
+{
+    int64_t sum = 0;
+    // queries that see a strict prefix of the tile: ks <= i <= ks+L-2, count i-ks+1
+    const int64_t lo = qa > ks ? qa : ks;
+    const int64_t hi = (qb - 1) < (ks + L - 2) ? (qb - 1) : (ks + L - 2);
+    if (lo <= hi) {
+        const int64_t x1 = lo - ks + 1, x2 = hi - ks + 1;
+        sum += (x1 + x2) * (x2 - x1 + 1) / 2;
+    }
+    // queries that see the whole tile: i >= ks+L-1
+    const int64_t full_lo = qa > (ks + L - 1) ? qa : (ks + L - 1);
+    if (qb > full_lo) sum += L * (qb - full_lo);
+    return sum;
+}
+
+int fwd_common(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+               int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype, float scale,
+               int rank_lo, int rank_hi, void *stream)
+{
+    if (B < 0 || Hq < 1 || Hkv < 1 || (causal != 0 && causal != 1)) return CP_EINVAL;
+    int rc = check_shard(S, N, layout);
+    if (rc) return rc;
+    if (Hq % Hkv) return CP_EINVAL;
+    if (rank_lo < 0 || rank_hi > N || rank_lo >= rank_hi) return CP_EINVAL;
+    if (dtype != CP_F32 && dtype != CP_BF16) return CP_EUNSUPPORTED;
+    if (D != 64 && D != 128) return CP_EUNSUPPORTED;
+    if (B == 0 || S == 0) return CP_OK;
+    if (!q || !k || !v || !out || !lse) return CP_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || ((uintptr_t)lse & 3u))
+        return CP_EINVAL;
+    FwdArgs a;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.S = (int)S;
+    a.D = D;
+    a.N = N;
+    a.causal = causal;
+    a.layout = layout;
+    a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    a.rank_lo = rank_lo;
+    a.rank_hi = rank_hi;
+    a.upc = 0;
+    a.err = err_ptr();
+    a.limit_ns = WAIT_LIMIT_NS;
+    if (!a.err) return CP_ECUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == CP_F32)
+        return launch_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                              static_cast<const float *>(v), static_cast<float *>(out), lse, a, st);
+    return launch_fwd_bf16(q, k, v, out, lse, a, st);
+}
+
+}  // namespace
+
+int sm_count()
+{
+    static int counts[MAX_DEV] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return 148;
+    if (!counts[dev]) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1)
+            c = 148;
+        counts[dev] = c;
+    }
+    return counts[dev];
+}
+
+}  // namespace cp
+
+using namespace cp;
+
+extern "C" {
+
+int cp_shard_map(int64_t S, int N, int layout, int32_t *pos_host)
+{
+    if (!pos_host) return CP_EINVAL;
+    int rc = check_shard(S, N, layout);
+    if (rc) return rc;
+    if (S == 0) return CP_OK;
+    const Geom g = make_geom((int)S, N, layout, 1);
+    const int L = (int)(S / N);
+    for (int r = 0; r < N; ++r)
+        for (int t = 0; t < L; ++t) pos_host[(int64_t)r * L + t] = shard_pos(g, r, t);
+    return CP_OK;
+}
+
+int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_host,
+                      int64_t *tiles_host)
+{
+    if (!pairs_host) return CP_EINVAL;
+    int rc = check_shard(S, N, layout);
+    if (rc) return rc;
+    for (int i = 0; i < N * N; ++i) {
+        pairs_host[i] = 0;
+        if (tiles_host) tiles_host[i] = 0;
+    }
+    if (S == 0) return CP_OK;
+    // Walk the units and KV tiles of the bf16 kernel (two 128-row query tiles
+    // per unit, 128-key KV tiles) and count what each query tile covers.
+    constexpr int QROWS = 256, T = 128;
+    const Geom g = make_geom((int)S, N, layout, causal);
+    const int upc = (g.clen + QROWS - 1) / QROWS;
+    const int units = num_selected_chunks(g, 0, N) * upc;
+    for (int u = 0; u < units; ++u) {
+        const Unit w = decode_unit(g, 1, 1, 0, N, upc, QROWS, u);
+        KvIter<T> it;
+        it.begin(g, w.r, w.qmax);
+        for (; it.valid(); it.next()) {
+            const int64_t ks = it.start(), ke = ks + it.len();   // keys [ks, ke)
+            for (int qi = 0; qi < 2; ++qi) {
+                const int64_t qa = w.q0 + (int64_t)qi * T;
+                int64_t qb = qa + T;                           // queries [qa, qb)
+                if (qb > w.cend) qb = w.cend;
+                if (qa >= qb) continue;
+                const int64_t p = causal ? visible_pairs(qa, qb, ks, ke - ks) : (qb - qa) * (ke - ks);
+                pairs_host[w.r * N + it.k] += p;
+                if (tiles_host) tiles_host[w.r * N + it.k] += 1;
+            }
+        }
+    }
+    return CP_OK;
+}
+
+int ring_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                  int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype,
+                  float scale, void *stream)
+{
+    return fwd_common(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, layout, dtype, scale, 0, N,
+                      stream);
+}
+
+int ring_attn_fwd_rank(const void *q, const void *k, const void *v, void *out, float *lse,
+                       int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout,
+                       int dtype, float scale, int rank_lo, int rank_hi, void *stream)
+{
+    return fwd_common(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, layout, dtype, scale,
+                      rank_lo, rank_hi, stream);
+}
+
+int lse_merge(const float *out_a, const float *lse_a, const float *out_b, const float *lse_b,
+              float *out, float *lse, int64_t rows, int D, void *stream)
+{
+    if (rows < 0 || D < 4 || D % 4) return CP_EINVAL;
+    if (rows == 0) return CP_OK;
+    if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse) return CP_EINVAL;
+    if (!aligned16(out_a) || !aligned16(out_b) || !aligned16(out)) return CP_EINVAL;
+    if (((uintptr_t)lse_a | (uintptr_t)lse_b | (uintptr_t)lse) & 3u) return CP_EINVAL;
+    return launch_lse_merge(out_a, lse_a, out_b, lse_b, out, lse, rows, D,
+                            static_cast<cudaStream_t>(stream));
+}
+
+static int ulysses_common(const void *src, void *dst, int B, int64_t S, int H, int D, int N,
+                          int layout, int elem_bytes, int to_head, void *stream)
+{
+    if (B < 0 || H < 1 || D < 1) return CP_EINVAL;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) return CP_EINVAL;
+    int rc = check_shard(S, N, layout);
+    if (rc) return rc;
+    if (H % N) return CP_EHEADS;
+    if (B == 0 || S == 0) return CP_OK;
+    if (!src || !dst) return CP_EINVAL;
+    return launch_ulysses(src, dst, B, (int)S, H, D, N, layout, elem_bytes, to_head,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_seq_to_head(const void *x, void *y, int B, int64_t S, int H, int D, int N,
+                        int layout, int elem_bytes, void *stream)
+{
+    return ulysses_common(x, y, B, S, H, D, N, layout, elem_bytes, 1, stream);
+}
+
+int ulysses_head_to_seq(const void *y, void *x, int B, int64_t S, int H, int D, int N,
+                        int layout, int elem_bytes, void *stream)
+{
+    return ulysses_common(y, x, B, S, H, D, N, layout, elem_bytes, 0, stream);
+}
+
+int cp_get_error(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CP_ECUDA;
+    unsigned w = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return CP_ECUDA;
+    if (w && cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return CP_ECUDA;
+    if (w == ERRW_TIMEOUT) return CP_ETIMEOUT;
+    return w ? CP_ECUDA : CP_OK;
+}
+
+const char *cp_strerror(int code)
+{
+    switch (code) {
+    case CP_OK: return "ok";
+    case CP_EINVAL: return "invalid argument (null pointer, size, divisibility or alignment)";
+    case CP_EHEADS: return "head count not divisible by the number of ranks (P <= H ceiling)";
+    case CP_EUNSUPPORTED: return "unsupported dtype, head dimension or shape";
+    case CP_ECUDA: return "CUDA runtime or launch failure";
+    case CP_ETIMEOUT: return "a device-side bounded wait ran out; outputs are undefined";
+    default: return "unknown status code";
+    }
+}
+
+int cp_debug_wait_timeout(uint64_t limit_ns, void *stream)
+{
+    if (limit_ns < 1000ull) limit_ns = 1000ull;
+    if (limit_ns > 5000000000ull) limit_ns = 5000000000ull;
+    unsigned *e = err_ptr();
+    if (!e) return CP_ECUDA;
+    return launch_debug_wait(e, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

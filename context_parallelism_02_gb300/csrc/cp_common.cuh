@@ -1,0 +1,326 @@
+// cp_common.cuh -- sequence sharding, ring schedule and tile classifier shared
+// by the host entry points and the device kernels of libcp, plus the small
+// device helpers every kernel uses (bounded mbarrier waits, error word).
+//
+// Sharding ("Sequence Parallelism in LLMs: Megatron-SP, Ulysses,
+// RingAttention", "Algorithmic Mechanics" step 1; "Context Parallelism",
+// "The causal imbalance"): the sequence is cut into chunks of equal length.
+// Contiguous: N chunks, rank r holds chunk r.  Zigzag: 2N chunks, rank r holds
+// chunks r and 2N-1-r (chunk r first in its local order).
+//
+// Ring schedule ("Algorithmic Mechanics" step 2; the ring sketch of "Context
+// Parallelism"): at step k = 0..N-1 rank r holds the KV shard of rank
+// (r - k) mod N and the causal mask is taken from that shard's global
+// positions ("Causal Masking and Load Balancing": key j visible to query i
+// iff j <= i).
+//
+// Tile classifier: a KV tile of the held shard whose first key lies after the
+// last query of the unit is fully masked and is never visited; a tile that
+// crosses the diagonal (or is cut short by the chunk end) is "partial" and is
+// masked element by element; every other tile is fully visible.
+#pragma once
+
+#include <stdint.h>
+
+#include "cp.h"
+
+#if defined(__CUDACC__)
+#define CP_HD __host__ __device__ __forceinline__
+#else
+#define CP_HD inline
+#endif
+
+namespace cp {
+
+// Error word values (per device, read and cleared by cp_get_error).
+constexpr unsigned ERRW_TIMEOUT = 1u;
+
+// All positions are int32: the library rejects S > INT32_MAX, and 32-bit
+// index arithmetic keeps the kernels free of 64-bit division routines.
+struct Geom {
+    int S;
+    int N;
+    int layout;
+    int causal;
+    int clen;       // chunk length: S/N (contiguous) or S/(2N) (zigzag)
+    int cpr;        // chunks per rank: 1 or 2
+};
+
+CP_HD Geom make_geom(int S, int N, int layout, int causal)
+{
+    Geom g;
+    g.S = S;
+    g.N = N;
+    g.layout = layout;
+    g.causal = causal;
+    g.cpr = (layout == CP_LAYOUT_ZIGZAG) ? 2 : 1;
+    g.clen = S / (N * g.cpr);
+    return g;
+}
+
+// i-th chunk (0 or 1) held by rank r.
+CP_HD int rank_chunk(const Geom &g, int r, int i)
+{
+    return (g.layout == CP_LAYOUT_ZIGZAG && i == 1) ? 2 * g.N - 1 - r : r;
+}
+
+// Rank holding chunk ch.
+CP_HD int chunk_rank(const Geom &g, int ch)
+{
+    return (g.layout == CP_LAYOUT_ZIGZAG && ch >= g.N) ? 2 * g.N - 1 - ch : ch;
+}
+
+// Global position of local row t of rank r.
+CP_HD int shard_pos(const Geom &g, int r, int t)
+{
+    int i = t / g.clen;
+    return rank_chunk(g, r, i) * g.clen + (t - i * g.clen);
+}
+
+CP_HD int ring_source(int N, int r, int k)
+{
+    int s = (r - k) % N;
+    return s < 0 ? s + N : s;
+}
+
+// Chunks of the ranks [lo, hi), listed by descending global position.  With a
+// causal mask a query's work grows with its position, so walking units in this
+// order hands out the longest work first.
+CP_HD int num_selected_chunks(const Geom &g, int lo, int hi) { return (hi - lo) * g.cpr; }
+
+CP_HD int selected_chunk(const Geom &g, int lo, int hi, int idx)
+{
+    int nr = hi - lo;
+    if (g.layout == CP_LAYOUT_ZIGZAG)
+        return idx < nr ? 2 * g.N - 1 - lo - idx : hi - 1 - (idx - nr);
+    return hi - 1 - idx;
+}
+
+// Number of TILE-key tiles of chunk [cstart, cstart+clen) that a unit whose
+// last query is qmax must visit.
+template <int TILE>
+CP_HD int tiles_needed(const Geom &g, int cstart, int qmax)
+{
+    int ntiles = (g.clen + TILE - 1) / TILE;
+    if (!g.causal) return ntiles;
+    if (qmax < cstart) return 0;
+    int n = (qmax - cstart) / TILE + 1;
+    return n < ntiles ? n : ntiles;
+}
+
+// Walks the KV tiles a unit of queries (held by rank r, last query qmax)
+// visits, in ring order: steps k = 0..N-1, the source's chunks in local order,
+// tiles in increasing position.
+template <int TILE>
+struct KvIter {
+    Geom g;
+    int r, qmax;
+    int k, ci;
+    int t, nt, cstart, cend;
+
+    CP_HD void begin(const Geom &g_, int r_, int qmax_)
+    {
+        g = g_;
+        r = r_;
+        qmax = qmax_;
+        k = 0;
+        ci = -1;
+        t = nt = cstart = cend = 0;
+        advance_chunk();
+    }
+    CP_HD bool advance_chunk()
+    {
+        for (;;) {
+            ++ci;
+            if (ci >= g.cpr) {
+                ci = 0;
+                ++k;
+            }
+            if (k >= g.N) return false;
+            int src = ring_source(g.N, r, k);
+            int ch = rank_chunk(g, src, ci);
+            cstart = ch * g.clen;
+            cend = cstart + g.clen;
+            nt = tiles_needed<TILE>(g, cstart, qmax);
+            t = 0;
+            if (nt > 0) return true;
+        }
+    }
+    CP_HD bool valid() const { return k < g.N; }
+    CP_HD int start() const { return cstart + t * TILE; }
+    CP_HD int len() const
+    {
+        int l = cend - start();
+        return l < TILE ? l : TILE;
+    }
+    CP_HD void next()
+    {
+        if (++t >= nt) advance_chunk();
+    }
+    // Total tiles of the walk (closed form per chunk).
+    CP_HD static int count(const Geom &g, int r, int qmax)
+    {
+        int n = 0;
+        for (int k = 0; k < g.N; ++k) {
+            int src = ring_source(g.N, r, k);
+            for (int ci = 0; ci < g.cpr; ++ci)
+                n += tiles_needed<TILE>(g, rank_chunk(g, src, ci) * g.clen, qmax);
+        }
+        return n;
+    }
+};
+
+// A unit of work: `qrows` consecutive query rows of one chunk, for one
+// (batch, query head).  Units are numbered heads fastest, then batch, then by
+// descending position.
+struct Unit {
+    int b, h, r;
+    int q0;     // first query position
+    int cend;   // end of the unit's chunk (rows at or past it are not stored)
+    int qmax;   // last valid query position
+};
+
+CP_HD Unit decode_unit(const Geom &g, int B, int Hq, int lo, int hi, int upc, int qrows, int u)
+{
+    Unit w;
+    w.h = u % Hq;
+    int rest = u / Hq;
+    w.b = rest % B;
+    rest /= B;
+    int pu = rest % upc;
+    int cu = rest / upc;
+    int ch = selected_chunk(g, lo, hi, cu);
+    w.r = chunk_rank(g, ch);
+    int cstart = ch * g.clen;
+    w.cend = cstart + g.clen;
+    w.q0 = cstart + (upc - 1 - pu) * qrows;
+    int last = w.q0 + qrows;
+    if (last > w.cend) last = w.cend;
+    w.qmax = last - 1;
+    return w;
+}
+
+}  // namespace cp
+
+#if defined(__CUDACC__)
+namespace cp {
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Shared state of the bounded waits of one block.
+struct WaitCtl {
+    unsigned *err;          // device error word
+    volatile int *abort;    // block-wide "give up" flag in shared memory
+    uint64_t limit_ns;      // how long one wait may take
+};
+
+__device__ __forceinline__ void raise_timeout(const WaitCtl &w)
+{
+    *w.abort = 1;
+    atomicCAS(w.err, 0u, ERRW_TIMEOUT);
+}
+
+// Slow paths of the waits below: spin with try_wait, check the clock and the
+// block's abort flag every few rounds.  Kept out of line so that the fast path
+// costs no registers.
+static __device__ __forceinline__ bool wait1_slow(uint32_t bar, uint32_t parity, WaitCtl w)
+{
+    uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*w.abort) return false;
+        if (globaltimer() - t0 > w.limit_ns) {
+            raise_timeout(w);
+            return false;
+        }
+    }
+}
+
+static __device__ __forceinline__ bool waitw_slow(uint32_t bar, uint32_t parity, WaitCtl w)
+{
+    const unsigned FULL = 0xffffffffu;
+    uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+        int give_up = 0;
+        if ((threadIdx.x & 31) == 0) {
+            if (*w.abort) give_up = 1;
+            else if (globaltimer() - t0 > w.limit_ns) {
+                raise_timeout(w);
+                give_up = 1;
+            }
+        }
+        if (__shfl_sync(FULL, give_up, 0)) return false;
+    }
+}
+
+// Single-thread bounded wait on phase `parity` of an mbarrier.  Returns false
+// when the limit ran out (the error word is set) or another thread gave up.
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtl &w)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait1_slow(bar, parity, w);
+}
+
+// Warp-collective bounded wait: every lane observes the phase, and the
+// outcome is the same on all lanes (so .sync.aligned instructions that follow
+// never diverge).
+__device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const WaitCtl &w)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    return waitw_slow(bar, parity, w);
+}
+
+}  // namespace cp
+#endif

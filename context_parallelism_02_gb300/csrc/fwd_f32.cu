@@ -1,0 +1,146 @@
+// fwd_f32.cu -- fp32 ring-attention forward on the FFMA pipes.
+//
+// The fp32 path has to agree with an fp64 reference to ~1e-5, which rules out
+// the tf32 tensor-core kinds, so this kernel computes everything in fp32 on
+// the CUDA cores with precise expf/logf.  It walks exactly the ring schedule
+// of the bf16 kernel ("Algorithmic Mechanics": step k uses the KV shard of
+// rank (i-k) mod P; flash_block of the "Context Parallelism" ring sketch) with
+// 16-row query units and 32-key KV tiles, and folds every tile into the
+// running (O, m, l) with the online-softmax rescaling equations of
+// "Algorithmic Mechanics".
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "cp_common.cuh"
+#include "kernels.h"
+
+namespace cp {
+
+namespace {
+
+constexpr int QR = 16;      // query rows per unit
+constexpr int TK = 32;      // keys per KV tile
+constexpr int WARPS = 8;
+constexpr int ROWS_PER_WARP = QR / WARPS;
+
+template <int D>
+__global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__restrict__ q,
+                                                             const float *__restrict__ k,
+                                                             const float *__restrict__ v,
+                                                             float *__restrict__ out,
+                                                             float *__restrict__ lse,
+                                                             FwdArgs a)
+{
+    constexpr int DPL = D / 32;   // output elements per lane
+    __shared__ float Qs[QR][D];
+    __shared__ float Ks[TK][D + 1];
+    __shared__ float Vs[TK][D];
+
+    const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
+    const Unit w = decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QR, blockIdx.x);
+    const int grp = a.Hq / a.Hkv;
+    const int kvh = w.h / grp;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // load the query rows of the unit (rows past the chunk end are zero)
+    for (int i = threadIdx.x; i < QR * D; i += blockDim.x) {
+        int rr = i / D, d = i % D;
+        int pos = w.q0 + rr;
+        Qs[rr][d] = (pos < w.cend) ? q[(((int64_t)w.b * a.S + pos) * a.Hq + w.h) * D + d] : 0.f;
+    }
+
+    float o[ROWS_PER_WARP][DPL];
+    float m[ROWS_PER_WARP], l[ROWS_PER_WARP];
+#pragma unroll
+    for (int i = 0; i < ROWS_PER_WARP; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+    }
+
+    KvIter<TK> it;
+    it.begin(g, w.r, w.qmax);
+    for (; it.valid(); it.next()) {
+        const int ks = it.start();
+        const int kl = it.len();
+        __syncthreads();
+        for (int i = threadIdx.x; i < TK * D; i += blockDim.x) {
+            int j = i / D, d = i % D;
+            float kv = 0.f, vv = 0.f;
+            if (j < kl) {
+                int64_t off = (((int64_t)w.b * a.S + ks + j) * a.Hkv + kvh) * D + d;
+                kv = k[off];
+                vv = v[off];
+            }
+            Ks[j][d] = kv;
+            Vs[j][d] = vv;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < ROWS_PER_WARP; ++i) {
+            const int rr = warp * ROWS_PER_WARP + i;
+            const int qpos = w.q0 + rr;
+            // lane j scores key j
+            float s = 0.f;
+#pragma unroll 8
+            for (int d = 0; d < D; ++d) s = fmaf(Qs[rr][d], Ks[lane][d], s);
+            s *= a.scale;
+            const bool vis = lane < kl && (!a.causal || ks + lane <= qpos);
+            if (!vis) s = -INFINITY;
+            float mt = s;
+#pragma unroll
+            for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            const float mn = fmaxf(m[i], mt);
+            if (mn == -INFINITY) continue;   // nothing visible yet: state unchanged
+            const float alpha = expf(m[i] - mn);
+            const float p = vis ? expf(s - mn) : 0.f;
+            float ps = p;
+#pragma unroll
+            for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            l[i] = l[i] * alpha + ps;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[i][e] *= alpha;
+#pragma unroll 4
+            for (int j = 0; j < TK; ++j) {
+                const float pj = __shfl_sync(0xffffffffu, p, j);
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[i][e] = fmaf(pj, Vs[j][lane + 32 * e], o[i][e]);
+            }
+            m[i] = mn;
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < ROWS_PER_WARP; ++i) {
+        const int rr = warp * ROWS_PER_WARP + i;
+        const int qpos = w.q0 + rr;
+        if (qpos >= w.cend) continue;
+        const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+        float *orow = out + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) orow[lane + 32 * e] = o[i][e] * inv;
+        if (lane == 0)
+            lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] = l[i] > 0.f ? m[i] + logf(l[i]) : -INFINITY;
+    }
+}
+
+}  // namespace
+
+int launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse,
+                   FwdArgs a, cudaStream_t st)
+{
+    const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
+    a.upc = (g.clen + QR - 1) / QR;
+    const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
+    if (units == 0) return CP_OK;
+    if (units > 0x7fffffffLL) return CP_EUNSUPPORTED;
+    dim3 grid((unsigned)units), block(WARPS * 32);
+    if (a.D == 64)
+        fwd_f32_kernel<64><<<grid, block, 0, st>>>(q, k, v, out, lse, a);
+    else
+        fwd_f32_kernel<128><<<grid, block, 0, st>>>(q, k, v, out, lse, a);
+    return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
+}
+
+}  // namespace cp

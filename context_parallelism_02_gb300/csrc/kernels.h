@@ -1,0 +1,35 @@
+// kernels.h -- launchers shared between the C-ABI entry points (cp_api.cu)
+// and the kernel translation units.  Internal to libcp.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cp {
+
+struct FwdArgs {
+    int B, Hq, Hkv;
+    int S;                // sequence length (<= INT32_MAX)
+    int D, N, causal, layout;
+    float scale;          // softmax scale
+    int rank_lo, rank_hi; // virtual ranks whose queries are computed
+    int upc;              // query units per chunk (set by the launcher)
+    unsigned *err;        // device error word
+    uint64_t limit_ns;    // bound of every device-side wait
+};
+
+int launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse,
+                   FwdArgs a, cudaStream_t st);
+int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse,
+                    FwdArgs a, cudaStream_t st);
+int launch_lse_merge(const float *out_a, const float *lse_a, const float *out_b,
+                     const float *lse_b, float *out, float *lse, int64_t rows, int D,
+                     cudaStream_t st);
+int launch_ulysses(const void *src, void *dst, int B, int S, int H, int D, int N, int layout,
+                   int elem_bytes, int to_head, cudaStream_t st);
+int launch_debug_wait(unsigned *err, uint64_t limit_ns, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace cp

@@ -1,0 +1,104 @@
+// lse_merge.cu -- merge two normalised partial attention results.
+//
+// "Sequence Parallelism in LLMs", "Algorithmic Mechanics" (online softmax
+// rescaling): with each partial carried as (out_x, lse_x) = (O, m + ln l),
+// m = max(lse_a, lse_b), w_x = e^(lse_x - m) / (e^(lse_a - m) + e^(lse_b - m)),
+// out = w_a out_a + w_b out_b and lse = m + ln(e^(lse_a - m) + e^(lse_b - m)).
+// An empty partial (lse = -inf) gets weight 0; two empty partials give
+// (0, -inf).
+//
+// HBM-bound: per row it reads 2 rows of D floats + 2 lse and writes one row +
+// one lse.  One warp per row, 16-byte vectors, two rows in flight per warp,
+// grid sized to fill every SM.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "cp_common.cuh"
+#include "kernels.h"
+
+namespace cp {
+
+namespace {
+
+struct Weights {
+    float wa, wb, lse;
+};
+
+__device__ __forceinline__ Weights merge_weights(float la, float lb)
+{
+    Weights r;
+    const float m = fmaxf(la, lb);
+    if (m == -INFINITY) {
+        r.wa = r.wb = 0.f;
+        r.lse = -INFINITY;
+        return r;
+    }
+    const float ea = expf(la - m), eb = expf(lb - m);
+    const float s = ea + eb;
+    r.wa = ea / s;
+    r.wb = eb / s;
+    r.lse = m + logf(s);
+    return r;
+}
+
+__device__ __forceinline__ float4 axpby(float wa, float4 a, float wb, float4 b)
+{
+    return make_float4(fmaf(wa, a.x, wb * b.x), fmaf(wa, a.y, wb * b.y), fmaf(wa, a.z, wb * b.z),
+                       fmaf(wa, a.w, wb * b.w));
+}
+
+__global__ void __launch_bounds__(256) lse_merge_kernel(const float4 *xa,
+                                                        const float *la,
+                                                        const float4 *xb,
+                                                        const float *lb, float4 *xo, float *lo,
+                                                        int64_t rows, int d4)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r0 = 2 * wid; r0 < rows; r0 += 2 * nw) {
+        const int64_t r1 = r0 + 1;
+        const bool two = r1 < rows;
+        const float a0 = la[r0], b0 = lb[r0];
+        const float a1 = two ? la[r1] : -INFINITY, b1 = two ? lb[r1] : -INFINITY;
+        for (int i = lane; i < d4; i += 32) {
+            const float4 va0 = xa[r0 * d4 + i], vb0 = xb[r0 * d4 + i];
+            float4 va1, vb1;
+            if (two) {
+                va1 = xa[r1 * d4 + i];
+                vb1 = xb[r1 * d4 + i];
+            }
+            const Weights w0 = merge_weights(a0, b0);
+            xo[r0 * d4 + i] = axpby(w0.wa, va0, w0.wb, vb0);
+            if (two) {
+                const Weights w1 = merge_weights(a1, b1);
+                xo[r1 * d4 + i] = axpby(w1.wa, va1, w1.wb, vb1);
+            }
+        }
+        // every lane has read la/lb of both rows before lane 0 overwrites them
+        __syncwarp();
+        if (lane == 0) {
+            lo[r0] = merge_weights(a0, b0).lse;
+            if (two) lo[r1] = merge_weights(a1, b1).lse;
+        }
+    }
+}
+
+}  // namespace
+
+int launch_lse_merge(const float *out_a, const float *lse_a, const float *out_b,
+                     const float *lse_b, float *out, float *lse, int64_t rows, int D,
+                     cudaStream_t st)
+{
+    if (rows == 0) return CP_OK;
+    const int64_t warps_needed = (rows + 1) / 2;
+    int64_t blocks = (warps_needed + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    lse_merge_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+        reinterpret_cast<const float4 *>(out_a), lse_a, reinterpret_cast<const float4 *>(out_b),
+        lse_b, reinterpret_cast<float4 *>(out), lse, rows, D / 4);
+    return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
+}
+
+}  // namespace cp

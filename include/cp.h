@@ -1,0 +1,177 @@
+/*
+ * cp.h -- C ABI of libcp: exact ring / context-parallel attention on one
+ * GB300 (sm_103a), with the N ranks of the ring emulated on the device.
+ *
+ * The operation is the ring attention of
+ *   - "Sequence Parallelism in LLMs: Megatron-SP, Ulysses, RingAttention"
+ *     (llms.blog), section "RingAttention and Blockwise Context Parallelism":
+ *     "Algorithmic Mechanics" (partitioning, ring iteration, online softmax
+ *     rescaling) and "Causal Masking and Load Balancing";
+ *   - "Context Parallelism" (aiwiki), sections "Ring attention" and "The
+ *     causal imbalance", and its ring sketch ring_attention(q, k, v, group)
+ *     calling flash_block(q, k, v, out, m, lse, source);
+ * which the pages state is exact: the result equals single-device attention
+ * ("Sequence and Context Parallelism" (praveentn.live), "What it does not
+ * change").
+ *
+ * Conventions shared by every call
+ *   - Tensors are BSHD in GLOBAL token order: q and out [B][S][Hq][D],
+ *     k and v [B][S][Hkv][D] (innermost D contiguous, no padding);
+ *     lse is [B][Hq][S] fp32, natural log.
+ *   - Query head h reads kv head h / (Hq / Hkv) (contiguous GQA groups).
+ *   - causal: key j is visible to query i iff j <= i, in global positions.
+ *   - layout: CP_LAYOUT_CONTIGUOUS splits S into N shards of S/N tokens;
+ *     CP_LAYOUT_ZIGZAG splits S into 2N chunks and gives rank r chunks r and
+ *     2N-1-r (local row order: chunk r first).
+ *   - Ring schedule: rank r at step k = 0..N-1 uses the KV shard of rank
+ *     (r - k) mod N; N compute steps (step 0 is the local block).
+ *   - Device pointers are caller-owned device memory (the library keeps no
+ *     reference after the call returns).  They must be 16-byte aligned.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Compute calls
+ *     are asynchronous on it and return after the launch.
+ *   - The library allocates no device memory.  It reports device-side
+ *     failures (a bounded wait that timed out) through a per-device error word
+ *     read by cp_get_error().
+ *   - Return value: CP_OK or a negative CP_E* code; never an exception.
+ */
+#ifndef CP_H_
+#define CP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define CP_OK 0
+#define CP_EINVAL (-1)        /* null pointer, bad size, divisibility, misalignment */
+#define CP_EHEADS (-2)        /* Ulysses: H not divisible by N (P <= H ceiling) */
+#define CP_EUNSUPPORTED (-3)  /* dtype / head dim / shape combination not built */
+#define CP_ECUDA (-4)         /* a CUDA runtime call or launch failed */
+#define CP_ETIMEOUT (-5)      /* a device-side bounded wait ran out (cp_get_error) */
+
+/* sequence layouts */
+#define CP_LAYOUT_CONTIGUOUS 0
+#define CP_LAYOUT_ZIGZAG 1
+
+/* element types of q, k, v, out (lse is always fp32) */
+#define CP_F32 0
+#define CP_BF16 1
+
+/*
+ * cp_shard_map -- global position of every local row of every rank.
+ * "Algorithmic Mechanics", step 1 (contiguous: rank i holds block i of size
+ * s/P) and "The causal imbalance" (zigzag: 2N chunks, rank i holds chunks i
+ * and 2N-1-i).
+ *   pos_host: HOST array of N*(S/N) int32, written as pos[r*(S/N) + t].
+ * Errors: CP_EINVAL if pos_host is NULL, N < 1, S % N (contiguous),
+ * S % (2N) (zigzag), S/N > INT32_MAX or an unknown layout.  Host only.
+ */
+int cp_shard_map(int64_t S, int N, int layout, int32_t *pos_host);
+
+/*
+ * cp_schedule_pairs -- walk the exact tile schedule that ring_attn_fwd
+ * executes and count, per (rank r, ring step k), the masked-in
+ * (query, key) pairs it covers and the 128x128 tile pairs it runs.
+ * "Causal Masking and Load Balancing": under a causal mask contiguous
+ * sharding is imbalanced; zigzag equalises the masked-in work per rank.
+ *   pairs_host: HOST int64 [N*N], pairs[r*N + k];
+ *   tiles_host: HOST int64 [N*N] executed tile pairs, or NULL.
+ * Errors: CP_EINVAL as for cp_shard_map.  Host only.
+ */
+int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_host,
+                      int64_t *tiles_host);
+
+/*
+ * ring_attn_fwd -- exact attention as ring attention computes it, N virtual
+ * ranks emulated in one launch.  Each rank's queries run N flash_block steps
+ * against the KV shard held at that step ("Context Parallelism", ring
+ * sketch: source = (rank - step) mod world), masked by global positions of
+ * that source ("Causal Masking and Load Balancing"), with the running
+ * (out, m, l) folded by online-softmax rescaling ("Algorithmic Mechanics").
+ * Fully masked 128x128 tile pairs are skipped, so executed work tracks the
+ * masked-in work.
+ *   q [B][S][Hq][D], k, v [B][S][Hkv][D]: device, dtype CP_F32 or CP_BF16.
+ *   out [B][S][Hq][D]: device, same dtype (bf16 rounded to nearest even).
+ *   lse [B][Hq][S]: device fp32, lse_i = ln sum_j exp(scale * q_i.k_j).
+ *   D in {64, 128}; Hq % Hkv == 0; scale <= 0 selects 1/sqrt(D).
+ *   CP_BF16 runs tcgen05 tensor-core kernels (bf16 operands, fp32
+ *   accumulation); CP_F32 runs an fp32 FFMA kernel.
+ * Errors: CP_EINVAL (null pointer, misalignment, B/Hq/Hkv/S/N < 1, S % N,
+ * S % 2N for zigzag, Hq % Hkv), CP_EUNSUPPORTED (D or dtype), CP_ECUDA.
+ */
+int ring_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                  int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype,
+                  float scale, void *stream);
+
+/*
+ * ring_attn_fwd_rank -- the same computation restricted to the queries held
+ * by virtual ranks [rank_lo, rank_hi): rows of other ranks in out and lse are
+ * left untouched.  Used to time each rank's share of the ring (the causal
+ * imbalance of "The causal imbalance").  Arguments and errors as
+ * ring_attn_fwd, plus CP_EINVAL unless 0 <= rank_lo < rank_hi <= N.
+ */
+int ring_attn_fwd_rank(const void *q, const void *k, const void *v, void *out, float *lse,
+                       int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout,
+                       int dtype, float scale, int rank_lo, int rank_hi, void *stream);
+
+/*
+ * lse_merge -- merge two normalised partial attention results over disjoint
+ * key sets ("Algorithmic Mechanics", online softmax rescaling, written with
+ * lse = m + ln l):  lse = ln(e^lse_a + e^lse_b),
+ * out = e^(lse_a - lse) out_a + e^(lse_b - lse) out_b.  An empty partial has
+ * lse = -inf and drops out; both empty gives (0, -inf).
+ *   out_a, out_b, out: device fp32 [rows][D]; lse_a, lse_b, lse: device fp32
+ *   [rows].  out may alias out_a or out_b, lse may alias lse_a or lse_b.
+ *   D % 4 == 0, rows >= 0 (rows == 0 is a no-op).
+ * Errors: CP_EINVAL (null pointer, misalignment, D), CP_ECUDA.
+ */
+int lse_merge(const float *out_a, const float *lse_a, const float *out_b, const float *lse_b,
+              float *out, float *lse, int64_t rows, int D, void *stream);
+
+/*
+ * ulysses_seq_to_head / ulysses_head_to_seq -- the two all-to-all relayouts
+ * of DeepSpeed-Ulysses done as one local permutation over all N ranks'
+ * buffers ("Sequence Parallelism in LLMs", "DeepSpeed Ulysses": [Batch, S/P,
+ * H, D] -> [Batch, S, H/P, D] and back).
+ *   x: rank-major stack of the N sequence shards, [N][B][S/N][H][D], rank r's
+ *      rows in the order of the sequence layout (cp_shard_map);
+ *   y: rank-major stack of the N head groups, [N][B][S][H/N][D]: rank g holds
+ *      heads [g*H/N, (g+1)*H/N) over the full sequence in global order.
+ *   elem_bytes in {1, 2, 4, 8}; pure byte copies (bit exact).
+ * Errors: CP_EHEADS if H % N != 0 (the head-count ceiling P <= H of
+ * "Communication Cost and Constraints"), CP_EINVAL (null pointer, S % N,
+ * S % 2N for zigzag, sizes), CP_ECUDA.
+ */
+int ulysses_seq_to_head(const void *x, void *y, int B, int64_t S, int H, int D, int N,
+                        int layout, int elem_bytes, void *stream);
+int ulysses_head_to_seq(const void *y, void *x, int B, int64_t S, int H, int D, int N,
+                        int layout, int elem_bytes, void *stream);
+
+/*
+ * cp_get_error -- synchronise `stream`, then read and clear the calling
+ * device's error word.  Returns CP_OK, CP_ETIMEOUT (a kernel's bounded wait
+ * ran out and the kernel returned early; its outputs are undefined) or
+ * CP_ECUDA (the synchronisation itself failed).
+ */
+int cp_get_error(void *stream);
+
+/* cp_strerror -- static description of a status code. */
+const char *cp_strerror(int code);
+
+/*
+ * cp_debug_wait_timeout -- test hook for the failure path: launches one
+ * block that waits on a shared-memory barrier nobody arrives at, with a
+ * wait limit of limit_ns nanoseconds (clamped to [1e3, 5e9]).  The wait runs
+ * out, the kernel records CP_ETIMEOUT in the error word and returns; the
+ * context stays usable.  Errors: CP_ECUDA.
+ */
+int cp_debug_wait_timeout(uint64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CP_H_ */

@@ -17,3 +17,28 @@ def oracle():
     import oracle as _oracle
     _oracle.build()
     return _oracle
+
+
+# Tolerances (BASELINE workloads): bf16 inputs with fp32 accumulation,
+# fp32 inputs, and exact work for integer / byte paths.
+BF16_MAX = 1e-2
+BF16_MEAN = 1e-3
+BF16_LSE = 1e-3
+F32_TOL = 1e-5
+
+
+@pytest.fixture(scope="session")
+def cplib():
+    """libcp built in-tree (build() on the machine running the tests)."""
+    from context_parallelism_02_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+@pytest.fixture(scope="session")
+def cuda_dev(cplib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")

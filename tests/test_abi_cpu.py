@@ -1,0 +1,105 @@
+"""CPU-side checks of the C ABI: the library loads, exports every entry point
+that include/cp.h declares, and its host-only calls (shard map, schedule walk,
+argument validation) behave as documented.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from context_parallelism_02_gb300 import _lib, api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CONT, ZIG = 0, 1
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "cp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(cplib):
+    names = _declared_symbols()
+    assert {"ring_attn_fwd", "lse_merge", "ulysses_seq_to_head", "ulysses_head_to_seq",
+            "cp_shard_map", "cp_get_error"} <= set(names)
+    for n in names:
+        assert hasattr(cplib, n), n
+    # the Python binding knows the same set
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_library_is_in_tree(cplib):
+    assert os.path.realpath(_lib.lib_path()).startswith(os.path.realpath(ROOT))
+
+
+@pytest.mark.parametrize("S,N,layout", [(8192, 8, CONT), (64, 4, ZIG), (1600, 4, ZIG),
+                                        (1000, 4, CONT), (48, 1, ZIG)])
+def test_shard_map_matches_oracle(cplib, oracle, S, N, layout):
+    np.testing.assert_array_equal(api.cp_shard_map(S, N, layout), oracle.shard_pos(S, N, layout))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("S,N,layout", [(512, 4, CONT), (512, 4, ZIG), (8192, 8, ZIG),
+                                        (8192, 8, CONT), (1600, 4, ZIG), (1000, 4, CONT),
+                                        (384, 1, ZIG), (96, 3, CONT)])
+def test_schedule_pairs_match_oracle(cplib, oracle, S, N, layout, causal):
+    """The kernel's tile schedule (tile skipping included) covers exactly the
+    masked-in pairs of every (rank, step): bit-exact integer counts."""
+    pairs, tiles = api.cp_schedule_pairs(S, N, layout, causal)
+    np.testing.assert_array_equal(pairs, oracle.pair_counts(S, N, layout, causal))
+    assert np.all(tiles >= 0)
+
+
+def test_schedule_long_sequence_closed_forms(cplib):
+    """S=131072, N=16: per-rank masked-in work, contiguous vs zigzag."""
+    S, N = 131072, 16
+    C, c = S // N, S // (2 * N)
+    pc, tc = api.cp_schedule_pairs(S, N, CONT, True)
+    pz, tz = api.cp_schedule_pairs(S, N, ZIG, True)
+    for r in range(N):
+        assert pc[r].sum() == r * C * C + C * (C + 1) // 2
+        assert pz[r].sum() == 2 * N * c * c + c
+    assert pc.sum() == pz.sum() == S * (S + 1) // 2
+    assert pc.sum(1)[0] == 33_558_528 and pc.sum(1)[-1] == 1_040_191_488
+    # executed tile pairs: equal per rank under zigzag; only diagonal tiles are partial
+    per_rank = tz.sum(1)
+    assert per_rank.max() - per_rank.min() <= 2
+    full_pairs = S * (S + 1) // 2
+    assert tz.sum() * 128 * 128 <= full_pairs * 1.01
+
+
+def _call_fwd(**kw):
+    a = dict(q=None, k=None, v=None, out=None, lse=None, B=1, Hq=2, Hkv=2, S=512, D=64, N=4,
+             causal=1, layout=ZIG, dtype=1, scale=-1.0, stream=None)
+    a.update(kw)
+    return _lib.load().ring_attn_fwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["Hq"],
+                                     a["Hkv"], a["S"], a["D"], a["N"], a["causal"], a["layout"],
+                                     a["dtype"], a["scale"], a["stream"])
+
+
+def test_argument_validation_without_gpu(cplib):
+    """Errors are returned before any CUDA call, so these run on a CPU-only box."""
+    assert _call_fwd(Hq=3, Hkv=2) == _lib.CP_EINVAL           # Hq % Hkv
+    assert _call_fwd(S=500, N=4) == _lib.CP_EINVAL            # zigzag needs S % 2N
+    assert _call_fwd(S=510, N=4, layout=CONT) == _lib.CP_EINVAL
+    assert _call_fwd(N=0) == _lib.CP_EINVAL
+    assert _call_fwd(layout=2) == _lib.CP_EINVAL
+    assert _call_fwd(D=96) == _lib.CP_EUNSUPPORTED
+    assert _call_fwd(dtype=7) == _lib.CP_EUNSUPPORTED
+    assert _call_fwd() == _lib.CP_EINVAL                      # null pointers
+    assert _call_fwd(B=0) == _lib.CP_OK                       # empty batch: no-op
+    assert _call_fwd(S=0) == _lib.CP_OK                       # empty sequence: no-op
+    L = _lib.load()
+    # Ulysses head ceiling (P <= H): 6 heads cannot be split over 4 ranks
+    assert L.ulysses_seq_to_head(None, None, 1, 64, 6, 8, 4, 0, 2, None) == _lib.CP_EHEADS
+    assert L.ulysses_head_to_seq(None, None, 1, 64, 8, 8, 4, 1, 2, None) == _lib.CP_EINVAL
+    assert L.ulysses_seq_to_head(None, None, 1, 64, 8, 8, 4, 0, 3, None) == _lib.CP_EINVAL
+    assert L.lse_merge(None, None, None, None, None, None, 0, 128, None) == _lib.CP_OK
+    assert L.lse_merge(None, None, None, None, None, None, 4, 6, None) == _lib.CP_EINVAL
+    buf = np.zeros(8, np.int32)
+    assert L.cp_shard_map(12, 4, ZIG, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL
+    assert L.cp_shard_map(1 << 40, 4, CONT, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert isinstance(_lib.strerror(code), str) and _lib.strerror(code)

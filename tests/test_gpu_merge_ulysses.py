@@ -1,0 +1,109 @@
+"""GPU parity of lse_merge, the Ulysses relayouts and the bounded-wait failure
+path, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from context_parallelism_02_gb300 import CP_ETIMEOUT, api, inputs
+from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, ZIGZAG as ZIG
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("rows,D,ninf", [(1, 128, 0), (1000, 128, 0), (4097, 64, 7), (65536, 128, 5),
+                                         (3, 4, 2)])
+def test_lse_merge_matches_oracle(cuda_dev, oracle, rows, D, ninf):
+    a, la, b, lb = inputs.make_merge_inputs(rows, D, seed=31, neg_inf_every=ninf)
+    if ninf:   # also a row where both partials are empty
+        la[0] = lb[0] = float("-inf")
+    out, lse = api.lse_merge(*(t.to(cuda_dev) for t in (a, la, b, lb)))
+    torch.cuda.synchronize()
+    ref, lref = oracle.lse_merge(a, la, b, lb)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.abs(out - ref).max() <= 1e-6
+    fin = np.isfinite(lref)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.abs(lse[fin] - lref[fin]).max(initial=0) <= 1e-6
+    if ninf:
+        assert np.all(out[0] == 0) and np.isneginf(lse[0])
+
+
+def test_lse_merge_in_place_and_full_size(cuda_dev, oracle):
+    """The benchmark workload (rows = 1x8x131072, D = 128), out aliasing out_a;
+    sampled rows checked against the oracle."""
+    a, la, b, lb = inputs.make_merge_inputs()
+    ga, gla, gb, glb = (t.to(cuda_dev) for t in (a, la, b, lb))
+    out, lse = api.lse_merge(ga, gla, gb, glb, out=ga, lse=gla)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(3).integers(0, la.numel(), 4096)
+    ref, lref = oracle.lse_merge(a[rows], la[rows], b[rows], lb[rows])
+    assert np.abs(out[rows].cpu().numpy() - ref).max() <= 1e-6
+    assert np.abs(lse[rows].cpu().numpy() - lref).max() <= 1e-6
+
+
+def test_lse_merge_equals_attention_over_split_keys(cuda_dev, oracle):
+    """Attention over keys [0, 40) and [40, S) merged equals attention over all."""
+    S, D = 96, 64
+    g = torch.Generator().manual_seed(5)
+    q, k, v = (torch.randn(1, S, 1, D, generator=g, dtype=torch.float64) for _ in range(3))
+    oa, la = oracle.attn_fwd(q, k, v, False, klo=0, khi=40)
+    ob, lb = oracle.attn_fwd(q, k, v, False, klo=40, khi=S)
+    full, lfull = oracle.attn_fwd(q, k, v, False)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x.reshape(-1, D) if x.ndim == 4 else x.reshape(-1))).float().to(cuda_dev)
+    out, lse = api.lse_merge(t(oa), t(la), t(ob), t(lb))
+    torch.cuda.synchronize()
+    assert np.abs(out.cpu().numpy() - full.reshape(-1, D)).max() <= 1e-5
+    assert np.abs(lse.cpu().numpy() - lfull.reshape(-1)).max() <= 1e-5
+
+
+ULY = [
+    # N, B, S, H, D, dtype, layout
+    (2, 1, 64, 4, 8, torch.bfloat16, CONT),
+    (4, 2, 128, 8, 16, torch.float32, ZIG),
+    (8, 1, 256, 8, 128, torch.bfloat16, ZIG),
+    (4, 1, 96, 4, 3, torch.bfloat16, CONT),      # 6-byte runs: narrow vectors
+    (1, 1, 32, 3, 8, torch.float32, ZIG),
+]
+
+
+@pytest.mark.parametrize("case", ULY)
+def test_ulysses_bit_exact(cuda_dev, oracle, case):
+    N, B, S, H, D, dt, layout = case
+    x = inputs.make_layout_tensor(N, B, S, H, D, dt, seed=41)
+    y = api.ulysses_seq_to_head(x.to(cuda_dev), N, layout)
+    torch.cuda.synchronize()
+    ref = oracle.ulysses_seq_to_head(x, N, layout)
+    assert np.array_equal(y.cpu().contiguous().view({2: torch.int16, 4: torch.int32}[x.element_size()]).numpy(), ref)
+    back = api.ulysses_head_to_seq(y, N, layout)
+    torch.cuda.synchronize()
+    assert torch.equal(back.cpu(), x)
+
+
+@pytest.mark.parametrize("name,H", [("q", 32), ("kv", 8)])
+def test_ulysses_gqa_workload(cuda_dev, oracle, name, H):
+    """The GQA workload's tensors (S=32768, N=8, zigzag): q [8][1][4096][32][128]
+    and k/v [8][1][4096][8][128] bf16, both directions, bit-exact."""
+    N, B, S, D = 8, 1, 32768, 128
+    x = inputs.make_layout_tensor(N, B, S, H, D, torch.bfloat16, seed=42)
+    gx = x.to(cuda_dev)
+    y = api.ulysses_seq_to_head(gx, N, ZIG)
+    back = api.ulysses_head_to_seq(y, N, ZIG)
+    torch.cuda.synchronize()
+    assert torch.equal(back, gx)
+    ref = oracle.ulysses_seq_to_head(x, N, ZIG)
+    assert np.array_equal(y.cpu().view(torch.int16).numpy(), ref)
+
+
+def test_bounded_wait_times_out_and_context_survives(cuda_dev):
+    """A wait on a barrier nothing arrives at gives up after its limit; the
+    error word reports CP_ETIMEOUT and the context keeps working."""
+    assert api.cp_get_error() == 0
+    api.cp_debug_wait_timeout(2_000_000)          # 2 ms
+    assert api.cp_get_error() == CP_ETIMEOUT
+    assert api.cp_get_error() == 0                # read clears it
+    w = inputs.TINY.with_(dtype=torch.bfloat16)
+    q, k, v = (t.to(cuda_dev) for t in inputs.make_qkv(w))
+    out, _ = api.ring_attn_fwd(q, k, v, w.N, w.layout, True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert api.cp_get_error() == 0
