@@ -1,8 +1,12 @@
 // fwd_f32.cu -- fp32 ring-attention forward on the FFMA pipes.
 //
-// The fp32 path has to agree with an fp64 reference to ~1e-5, which rules out
-// the tf32 tensor-core kinds, so this kernel computes everything in fp32 on
-// the CUDA cores with precise expf/logf.  It walks exactly the ring schedule
+// The fp32 path has to agree with an fp64 reference to ~1e-5 even with
+// logits of several tens (q scaled by 8), which rules out the tf32
+// tensor-core kinds and also plain fp32 dot products: a logit near 30 carries
+// an fp32 rounding error of ~2e-6, which a near one-hot softmax passes
+// straight into the output.  So this kernel reads and writes fp32 but forms
+// scores, the running max and sum, and the output accumulator in fp64 on the
+// CUDA cores.  It is the precision path, not the fast path.  It walks exactly the ring schedule
 // of the bf16 kernel ("Algorithmic Mechanics": step k uses the KV shard of
 // rank (i-k) mod P; flash_block of the "Context Parallelism" ring sketch) with
 // 16-row query units and 32-key KV tiles, and folds every tile into the
@@ -49,15 +53,16 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
         Qs[rr][d] = (pos < w.cend) ? q[(((int64_t)w.b * a.S + pos) * a.Hq + w.h) * D + d] : 0.f;
     }
 
-    float o[ROWS_PER_WARP][DPL];
-    float m[ROWS_PER_WARP], l[ROWS_PER_WARP];
+    double o[ROWS_PER_WARP][DPL];
+    double m[ROWS_PER_WARP], l[ROWS_PER_WARP];
 #pragma unroll
     for (int i = 0; i < ROWS_PER_WARP; ++i) {
         m[i] = -INFINITY;
-        l[i] = 0.f;
+        l[i] = 0.0;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+        for (int e = 0; e < DPL; ++e) o[i][e] = 0.0;
     }
+    const double scale = (double)a.scale;
 
     KvIter<TK> it;
     it.begin(g, w.r, w.qmax);
@@ -82,20 +87,20 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
             const int rr = warp * ROWS_PER_WARP + i;
             const int qpos = w.q0 + rr;
             // lane j scores key j
-            float s = 0.f;
+            double s = 0.0;
 #pragma unroll 8
-            for (int d = 0; d < D; ++d) s = fmaf(Qs[rr][d], Ks[lane][d], s);
-            s *= a.scale;
+            for (int d = 0; d < D; ++d) s = fma((double)Qs[rr][d], (double)Ks[lane][d], s);
+            s *= scale;
             const bool vis = lane < kl && (!a.causal || ks + lane <= qpos);
             if (!vis) s = -INFINITY;
-            float mt = s;
+            double mt = s;
 #pragma unroll
-            for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-            const float mn = fmaxf(m[i], mt);
+            for (int off = 16; off; off >>= 1) mt = fmax(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            const double mn = fmax(m[i], mt);
             if (mn == -INFINITY) continue;   // nothing visible yet: state unchanged
-            const float alpha = expf(m[i] - mn);
-            const float p = vis ? expf(s - mn) : 0.f;
-            float ps = p;
+            const double alpha = exp(m[i] - mn);
+            const double p = vis ? exp(s - mn) : 0.0;
+            double ps = p;
 #pragma unroll
             for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
             l[i] = l[i] * alpha + ps;
@@ -103,9 +108,9 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
             for (int e = 0; e < DPL; ++e) o[i][e] *= alpha;
 #pragma unroll 4
             for (int j = 0; j < TK; ++j) {
-                const float pj = __shfl_sync(0xffffffffu, p, j);
+                const double pj = __shfl_sync(0xffffffffu, p, j);
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) o[i][e] = fmaf(pj, Vs[j][lane + 32 * e], o[i][e]);
+                for (int e = 0; e < DPL; ++e) o[i][e] = fma(pj, (double)Vs[j][lane + 32 * e], o[i][e]);
             }
             m[i] = mn;
         }
@@ -116,12 +121,13 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
         const int rr = warp * ROWS_PER_WARP + i;
         const int qpos = w.q0 + rr;
         if (qpos >= w.cend) continue;
-        const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+        const double inv = l[i] > 0.0 ? 1.0 / l[i] : 0.0;
         float *orow = out + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) orow[lane + 32 * e] = o[i][e] * inv;
+        for (int e = 0; e < DPL; ++e) orow[lane + 32 * e] = (float)(o[i][e] * inv);
         if (lane == 0)
-            lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] = l[i] > 0.f ? m[i] + logf(l[i]) : -INFINITY;
+            lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] =
+                l[i] > 0.0 ? (float)(m[i] + log(l[i])) : -INFINITY;
     }
 }
 

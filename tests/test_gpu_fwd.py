@@ -83,11 +83,17 @@ def test_small_bf16(cuda_dev, oracle, case):
 
 
 def test_large_logit_bf16(cuda_dev, oracle):
-    """q scaled by 8: logits of tens, lse stays accurate (online rescaling)."""
+    """q scaled by 8: logits of tens, lse stays accurate (online rescaling).
+
+    Rows become nearly one-hot, so |out| reaches the size of single v entries
+    (up to ~4).  bf16 rounding of P and of out is relative (half an ulp is
+    2^-9), so here the 1e-2 bound is taken relative to max(1, |ref|)."""
     w = Workload("qx8", 1, 2, 2, 2048, 128, 4, ZIG, True, torch.bfloat16, seed=22, q_scale=8.0)
     q, k, v, out, lse = _run(w, cuda_dev)
     ref, lref = oracle.attn_fwd(q, k, v, True)
-    _check_bf16(out, lse, ref, lref, "qx8")
+    rel = np.abs(out - ref) / np.maximum(1.0, np.abs(ref))
+    assert rel.max() <= BF16_MAX and rel.mean() <= BF16_MEAN, (rel.max(), rel.mean())
+    assert np.abs(lse - lref).max() <= BF16_LSE
 
 
 def test_tiny_shape_bf16(cuda_dev, oracle):
