@@ -34,6 +34,9 @@ SIGNATURES = {
     "ring_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _P]),
     "ring_attn_fwd_rank": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _I,
                                 _I, _P]),
+    "ring_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I,
+                           _I, _F, _P, ctypes.c_size_t, _P]),
+    "ring_attn_bwd_workspace": (ctypes.c_size_t, [_I, _I, _L]),
     "lse_merge": (_I, [_P, _P, _P, _P, _P, _P, _L, _I, _P]),
     "ulysses_seq_to_head": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),
     "ulysses_head_to_seq": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),

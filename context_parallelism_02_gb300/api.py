@@ -88,6 +88,38 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, N: int, lay
     return out, lse
 
 
+def ring_attn_bwd_workspace(B: int, Hq: int, S: int) -> int:
+    return int(_lib.load().ring_attn_bwd_workspace(B, Hq, S))
+
+
+def ring_attn_bwd(q, k, v, out, lse, dout, N: int, layout: int, causal: bool = True,
+                  scale: float | None = None, dq=None, dk=None, dv=None, workspace=None,
+                  stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out) for :func:`ring_attn_fwd` (bf16).
+
+    ``workspace``: optional caller-owned device buffer of at least
+    ``ring_attn_bwd_workspace(B, Hq, S)`` bytes (allocated with torch if None).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout)):
+        _need_cuda_contig(name, t)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = ring_attn_bwd_workspace(B, Hq, S)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    sc = -1.0 if scale is None else float(scale)
+    rc = _lib.load().ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, S, D, N, int(causal),
+                                   layout, _DT[q.dtype], sc, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   ctypes.c_void_p(_stream(stream)))
+    check(rc, "ring_attn_bwd")
+    return dq, dk, dv
+
+
 def lse_merge(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
     """Merge two fp32 partials over disjoint key sets; returns (out, lse)."""
     for name, t in (("out_a", out_a), ("lse_a", lse_a), ("out_b", out_b), ("lse_b", lse_b)):

@@ -190,6 +190,50 @@ int ring_attn_fwd_rank(const void *q, const void *k, const void *v, void *out, f
                       rank_lo, rank_hi, stream);
 }
 
+size_t ring_attn_bwd_workspace(int B, int Hq, int64_t S)
+{
+    if (B < 0 || Hq < 0 || S < 0) return 0;
+    return bwd_workspace_bytes(B, Hq, S);
+}
+
+int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int64_t S,
+                  int D, int N, int causal, int layout, int dtype, float scale, void *workspace,
+                  size_t ws_bytes, void *stream)
+{
+    if (B < 0 || Hq < 1 || Hkv < 1 || (causal != 0 && causal != 1)) return CP_EINVAL;
+    int rc = check_shard(S, N, layout);
+    if (rc) return rc;
+    if (Hq % Hkv) return CP_EINVAL;
+    if (dtype != CP_BF16) return CP_EUNSUPPORTED;
+    if (D != 64 && D != 128) return CP_EUNSUPPORTED;
+    if (B == 0 || S == 0) return CP_OK;
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return CP_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+        ((uintptr_t)lse & 3u))
+        return CP_EINVAL;
+    if (ws_bytes < bwd_workspace_bytes(B, Hq, S)) return CP_EINVAL;
+    FwdArgs a;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.S = (int)S;
+    a.D = D;
+    a.N = N;
+    a.causal = causal;
+    a.layout = layout;
+    a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    a.rank_lo = 0;
+    a.rank_hi = N;
+    a.upc = 0;
+    a.err = err_ptr();
+    a.limit_ns = WAIT_LIMIT_NS;
+    if (!a.err) return CP_ECUDA;
+    BwdPtrs p{q, k, v, out, lse, dout, dq, dk, dv, workspace};
+    return launch_bwd_bf16(p, a, static_cast<cudaStream_t>(stream));
+}
+
 int lse_merge(const float *out_a, const float *lse_a, const float *out_b, const float *lse_b,
               float *out, float *lse, int64_t rows, int D, void *stream)
 {

@@ -200,6 +200,122 @@ CP_HD Unit decode_unit(const Geom &g, int B, int Hq, int lo, int hi, int upc, in
     return w;
 }
 
+// ---------------------------------------------------------------------------
+// Backward: key-stationary walk.  A KV tile of the shard of rank src receives
+// gradient from the queries of every rank r that holds it at some ring step,
+// r = (src + k) mod N for k = 0..N-1 (the same (rank, step) pairs the forward
+// visits), and from every query head of its GQA group.
+
+// Units of KV tiles: heads fastest, then batch, then tiles by ascending
+// position (under a causal mask early keys receive the most work).
+struct KvUnit {
+    int b, g;       // batch, kv head
+    int src;        // rank holding the tile's chunk
+    int ks;         // first key
+    int kl;         // valid keys in the tile
+    int kcend;      // end of the tile's chunk
+};
+
+template <int TILE>
+CP_HD KvUnit decode_kv_unit(const Geom &g, int B, int Hkv, int tpc, int u)
+{
+    KvUnit w;
+    w.g = u % Hkv;
+    int rest = u / Hkv;
+    w.b = rest % B;
+    rest /= B;
+    const int t = rest % tpc;
+    const int ch = rest / tpc;
+    w.src = chunk_rank(g, ch);
+    const int cstart = ch * g.clen;
+    w.kcend = cstart + g.clen;
+    w.ks = cstart + t * TILE;
+    const int l = w.kcend - w.ks;
+    w.kl = l < TILE ? l : TILE;
+    return w;
+}
+
+// Number of TILE-row query tiles of chunk [cstart, cend) that see key ks, and
+// the first of them.
+template <int TILE>
+CP_HD int qtiles_seeing(const Geom &g, int cstart, int ks, int &t0)
+{
+    const int ntiles = (g.clen + TILE - 1) / TILE;
+    t0 = 0;
+    if (!g.causal) return ntiles;
+    if (cstart + g.clen - 1 < ks) return 0;
+    if (ks - cstart > TILE - 1) t0 = (ks - cstart) / TILE;
+    return ntiles - t0;
+}
+
+// Walks the query tiles (head, ring step, chunk, tile) that see a KV tile.
+template <int TILE>
+struct QIter {
+    Geom g;
+    int src, ks, h0, grp;
+    int hh, k, ci, t, t0, nt, cstart, cend;
+
+    CP_HD void begin(const Geom &g_, int src_, int ks_, int h0_, int grp_)
+    {
+        g = g_;
+        src = src_;
+        ks = ks_;
+        h0 = h0_;
+        grp = grp_;
+        hh = 0;
+        k = 0;
+        ci = -1;
+        t = nt = t0 = cstart = cend = 0;
+        advance_chunk();
+    }
+    CP_HD bool advance_chunk()
+    {
+        for (;;) {
+            ++ci;
+            if (ci >= g.cpr) {
+                ci = 0;
+                ++k;
+                if (k >= g.N) {
+                    k = 0;
+                    ++hh;
+                }
+            }
+            if (hh >= grp) return false;
+            const int r = (src + k) % g.N;
+            const int ch = rank_chunk(g, r, ci);
+            cstart = ch * g.clen;
+            cend = cstart + g.clen;
+            nt = qtiles_seeing<TILE>(g, cstart, ks, t0);
+            t = 0;
+            if (nt > 0) return true;
+        }
+    }
+    CP_HD bool valid() const { return hh < grp; }
+    CP_HD int head() const { return h0 + hh; }
+    CP_HD int start() const { return cstart + (t0 + t) * TILE; }
+    CP_HD int len() const
+    {
+        const int l = cend - start();
+        return l < TILE ? l : TILE;
+    }
+    CP_HD void next()
+    {
+        if (++t >= nt) advance_chunk();
+    }
+    CP_HD static int count(const Geom &g, int src, int ks, int grp)
+    {
+        int n = 0;
+        for (int k = 0; k < g.N; ++k) {
+            const int r = (src + k) % g.N;
+            for (int ci = 0; ci < g.cpr; ++ci) {
+                int t0;
+                n += qtiles_seeing<TILE>(g, rank_chunk(g, r, ci) * g.clen, ks, t0);
+            }
+        }
+        return n * grp;
+    }
+};
+
 }  // namespace cp
 
 #if defined(__CUDACC__)

@@ -29,6 +29,16 @@ int launch_ulysses(const void *src, void *dst, int B, int S, int H, int D, int N
                    int elem_bytes, int to_head, cudaStream_t st);
 int launch_debug_wait(unsigned *err, uint64_t limit_ns, cudaStream_t st);
 
+struct BwdPtrs {
+    const void *q, *k, *v, *out;
+    const float *lse;
+    const void *dout;
+    void *dq, *dk, *dv;
+    void *workspace;   // Delta, bwd_workspace_bytes() bytes
+};
+int launch_bwd_bf16(const BwdPtrs &p, const FwdArgs &a, cudaStream_t st);
+size_t bwd_workspace_bytes(int B, int Hq, int64_t S);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

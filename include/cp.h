@@ -151,6 +151,34 @@ int ulysses_head_to_seq(const void *y, void *x, int B, int64_t S, int H, int D, 
                         int layout, int elem_bytes, void *stream);
 
 /*
+ * ring_attn_bwd -- gradients of L = sum(dout * out) for the ring forward
+ * above.  The pages state that context parallelism leaves the gradients equal
+ * to single-device training ("Sequence and Context Parallelism", "What it
+ * does not change") and give no backward algorithm; this is the textbook
+ * attention gradient with the saved lse, walked over the same (rank, ring
+ * step, tile) schedule as the forward:
+ *   P = exp(scale q.k - lse), Delta = rowsum(dout * out), dS = P (dout.v - Delta),
+ *   dq = scale dS k, dk = scale dS^T q, dv = P^T dout.
+ *   q, out, dout, dq [B][S][Hq][D]; k, v, dk, dv [B][S][Hkv][D]: device bf16.
+ *   lse [B][Hq][S] fp32: the forward's lse (natural log).
+ *   workspace: device, at least ring_attn_bwd_workspace(B, Hq, S) bytes,
+ *   16-byte aligned, caller-owned scratch (Delta); its contents on entry do
+ *   not matter and are overwritten.
+ *   Every output element is written exactly once (no atomics): the result is
+ *   deterministic.  dtype must be CP_BF16; D in {64, 128}.
+ * Errors: CP_EINVAL (as ring_attn_fwd, plus a null or too small workspace),
+ * CP_EUNSUPPORTED (dtype or D), CP_ECUDA.
+ */
+int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+                  int64_t S, int D, int N, int causal, int layout, int dtype, float scale,
+                  void *workspace, size_t ws_bytes, void *stream);
+
+/* ring_attn_bwd_workspace -- bytes of scratch ring_attn_bwd needs
+ * (B*Hq*S fp32, rounded up to 256 bytes); 0 for negative sizes.  Host only. */
+size_t ring_attn_bwd_workspace(int B, int Hq, int64_t S);
+
+/*
  * cp_get_error -- synchronise `stream`, then read and clear the calling
  * device's error word.  Returns CP_OK, CP_ETIMEOUT (a kernel's bounded wait
  * ran out and the kernel returned early; its outputs are undefined) or

@@ -1,0 +1,111 @@
+"""GPU parity of ring_attn_bwd (through the C ABI) against the fp64 oracle
+gradient.
+
+The pages give no gradient tolerance.  The bound used here follows from the
+arithmetic: P and dS are rounded to bf16 before the tensor-core products
+(relative half-ulp 2^-9) and dq/dk/dv are rounded to bf16 at the end, so the
+error of an output element is a small multiple of 2^-9 times the size of the
+gradient; with max|ref| the largest reference entry of the checked slice,
+max|err| <= 1e-2 * max|ref| and mean|err| <= 1e-3 * max|ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+from context_parallelism_02_gb300 import api, inputs
+from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, ZIGZAG as ZIG, Workload
+
+pytestmark = pytest.mark.gpu
+
+GRAD_MAX = 1e-2
+GRAD_MEAN = 1e-3
+
+
+def _grads(w, dev):
+    q, k, v, do = inputs.make_qkv(w)
+    gq, gk, gv, gdo = (t.to(dev) for t in (q, k, v, do))
+    out, lse = api.ring_attn_fwd(gq, gk, gv, w.N, w.layout, w.causal)
+    dq, dk, dv = api.ring_attn_bwd(gq, gk, gv, out, lse, gdo, w.N, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert api.cp_get_error() == 0
+    return (q, k, v, do), (dq.float().cpu().numpy(), dk.float().cpu().numpy(),
+                           dv.float().cpu().numpy())
+
+
+def _check(name, got, ref):
+    err = np.abs(got - ref)
+    scale = np.abs(ref).max()
+    assert np.isfinite(got).all(), name
+    assert err.max() <= GRAD_MAX * scale, (name, err.max(), scale)
+    assert err.mean() <= GRAD_MEAN * scale, (name, err.mean(), scale)
+
+
+SMALL = [
+    # name, B, Hq, Hkv, S, D, N, layout, causal
+    ("s1024_n4_zig", 1, 2, 2, 1024, 128, 4, ZIG, True),
+    ("gqa_ragged_c200", 2, 4, 2, 1600, 128, 4, ZIG, True),
+    ("d64_ragged_cont", 1, 2, 1, 1000, 64, 4, CONT, True),
+    ("noncausal_n2", 1, 2, 2, 1536, 128, 2, ZIG, False),
+    ("n1_plain", 1, 2, 2, 640, 128, 1, CONT, True),
+    ("chunk_below_tile", 1, 2, 2, 512, 64, 4, ZIG, True),
+    ("n8_zig", 1, 2, 2, 4096, 128, 8, ZIG, True),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_bwd(cuda_dev, oracle, case):
+    name, B, Hq, Hkv, S, D, N, layout, causal = case
+    w = Workload(name, B, Hq, Hkv, S, D, N, layout, causal, torch.bfloat16, seed=51,
+                 with_grad=True)
+    (q, k, v, do), (dq, dk, dv) = _grads(w, cuda_dev)
+    rows = np.arange(S)
+    rq, rk, rv = oracle.attn_bwd(q, k, v, do, causal, rows, rows)
+    _check(name + " dq", dq, rq)
+    _check(name + " dk", dk, rk)
+    _check(name + " dv", dv, rv)
+
+
+def test_bwd_deterministic_and_layout_free(cuda_dev):
+    """No atomics: two runs are bitwise equal; N and layout change only rounding."""
+    base = Workload("bdet", 1, 2, 2, 2048, 128, 4, ZIG, True, torch.bfloat16, seed=52,
+                    with_grad=True)
+    q, k, v, do = (t.to(cuda_dev) for t in inputs.make_qkv(base))
+    res = []
+    for N, layout in ((4, ZIG), (4, ZIG), (1, CONT), (8, CONT)):
+        out, lse = api.ring_attn_fwd(q, k, v, N, layout, True)
+        res.append(api.ring_attn_bwd(q, k, v, out, lse, do, N, layout, True))
+    torch.cuda.synchronize()
+    for a, b in zip(res[0], res[1]):
+        assert torch.equal(a, b)
+    for other in res[2:]:
+        for a, b in zip(res[0], other):
+            scale = a.float().abs().max()
+            assert (a.float() - b.float()).abs().max() <= 2 * GRAD_MAX * scale
+
+
+def test_bwd_full_size_slices_and_invariants(cuda_dev, oracle):
+    """B=2, H=16, S=32768, D=128, N=8, zigzag, causal.
+
+    Oracle gradient on slices: dq on 1024 query rows, dk/dv on the last 1024
+    keys (only the last queries see them), for two heads of both batches.
+    At full size, two identities of the exact gradient: since every row of P
+    sums to 1, sum_j dV_j = sum_i dO_i, and since sum_j dS_ij = 0 for every i,
+    sum_j dK_j = 0 (per batch and head)."""
+    w = inputs.BWD32K
+    (q, k, v, do), (dq, dk, dv) = _grads(w, cuda_dev)
+    heads = [0, 5]
+    sq, sk, sv, sdo = (t[:, :, heads] for t in (q, k, v, do))
+    rng = np.random.default_rng(7)
+    qrows = np.sort(rng.choice(w.S, 1024, replace=False))
+    krows = np.arange(w.S - 1024, w.S)
+    rq, rk, rv = oracle.attn_bwd(sq, sk, sv, sdo, True, qrows, krows)
+    _check("dq slice", dq[:, qrows][:, :, heads], rq)
+    _check("dk slice", dk[:, krows][:, :, heads], rk)
+    _check("dv slice", dv[:, krows][:, :, heads], rv)
+    # identities at full size (fp64 sums of the bf16 results)
+    sdv = dv.astype(np.float64).sum(axis=1)
+    sdo_ = do.double().numpy().sum(axis=1)
+    tol = 1e-2 * np.abs(sdo_).max()
+    assert np.abs(sdv - sdo_).max() <= tol, np.abs(sdv - sdo_).max()
+    sdk = dk.astype(np.float64).sum(axis=1)
+    assert np.abs(sdk).max() <= 1e-2 * np.abs(dk).max() * np.sqrt(w.S), np.abs(sdk).max()
