@@ -22,6 +22,7 @@ CP_LAYOUT_CONTIGUOUS = 0
 CP_LAYOUT_ZIGZAG = 1
 CP_F32 = 0
 CP_BF16 = 1
+CP_BWD_NOALLOC_MAX_ROWS = 4 * 1024 * 1024
 
 # name -> (restype, argtypes); mirrors include/cp.h
 _P = ctypes.c_void_p
@@ -37,6 +38,8 @@ SIGNATURES = {
     "ring_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I,
                            _I, _F, _P, ctypes.c_size_t, _P]),
     "ring_attn_bwd_workspace": (ctypes.c_size_t, [_I, _I, _L]),
+    "ring_attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I,
+                                   _I, _I, _I, _F, _P]),
     "lse_merge": (_I, [_P, _P, _P, _P, _P, _P, _L, _I, _P]),
     "ulysses_seq_to_head": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),
     "ulysses_head_to_seq": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),

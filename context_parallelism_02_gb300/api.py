@@ -120,6 +120,29 @@ def ring_attn_bwd(q, k, v, out, lse, dout, N: int, layout: int, causal: bool = T
     return dq, dk, dv
 
 
+def ring_attn_bwd_noalloc(q, k, v, out, lse, dout, N: int, layout: int, causal: bool = True,
+                          scale: float | None = None, dq=None, dk=None, dv=None, stream=None):
+    """:func:`ring_attn_bwd` without a workspace, for callers that cannot
+    allocate device memory: the library keeps the scratch in a fixed 16 MiB
+    device array (B * Hq * S <= CP_BWD_NOALLOC_MAX_ROWS).  Pass dq, dk, dv to
+    keep this call free of allocations (torch allocates them here otherwise).
+    Calls that overlap on the GPU share that array and race."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout)):
+        _need_cuda_contig(name, t)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    sc = -1.0 if scale is None else float(scale)
+    rc = _lib.load().ring_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                           _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv,
+                                           S, D, N, int(causal), layout, _DT[q.dtype], sc,
+                                           ctypes.c_void_p(_stream(stream)))
+    check(rc, "ring_attn_bwd_noalloc")
+    return dq, dk, dv
+
+
 def lse_merge(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
     """Merge two fp32 partials over disjoint key sets; returns (out, lse)."""
     for name, t in (("out_a", out_a), ("lse_a", lse_a), ("out_b", out_b), ("lse_b", lse_b)):

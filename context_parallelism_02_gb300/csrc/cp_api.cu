@@ -104,6 +104,10 @@ int fwd_common(const void *q, const void *k, const void *v, void *out, float *ls
 
 }  // namespace
 
+unsigned *device_error_word() { return err_ptr(); }
+
+uint64_t device_wait_limit_ns() { return WAIT_LIMIT_NS; }
+
 int sm_count()
 {
     static int counts[MAX_DEV] = {};

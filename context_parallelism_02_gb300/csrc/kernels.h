@@ -42,4 +42,9 @@ size_t bwd_workspace_bytes(int B, int Hq, int64_t S);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Device address of the current device's error word (set up once per device),
+// and the bound every device-side wait uses.
+unsigned *device_error_word();
+uint64_t device_wait_limit_ns();
+
 }  // namespace cp

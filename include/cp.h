@@ -179,6 +179,30 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
 size_t ring_attn_bwd_workspace(int B, int Hq, int64_t S);
 
 /*
+ * ring_attn_bwd_noalloc -- ring_attn_bwd for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this exists for code that
+ * may only use buffers handed to it (a plugin inside another framework, a
+ * caller bound to a memory pool or a fixed budget) and so has no way to
+ * provide ring_attn_bwd's workspace.  Same arguments, layouts and results as
+ * ring_attn_bwd, minus the workspace: the scratch (one fp32 per
+ * (batch, query head, position)) lives in a 16 MiB array compiled into the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.  The call allocates nothing.
+ *   Limit: B * Hq * S <= CP_BWD_NOALLOC_MAX_ROWS, else CP_EINVAL (nothing is
+ *   launched).
+ *   The first call on a device looks up the array's device address (one
+ *   runtime query, with that device current); make it before any stream
+ *   capture.  All calls on a device share the array: calls whose kernels
+ *   overlap on the GPU race.  Nothing in it needs clearing between calls.
+ * Errors: as ring_attn_bwd, plus CP_EINVAL for sizes beyond the limit.
+ */
+#define CP_BWD_NOALLOC_MAX_ROWS (4 * 1024 * 1024)
+int ring_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *out,
+                          const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                          int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout,
+                          int dtype, float scale, void *stream);
+
+/*
  * cp_get_error -- synchronise `stream`, then read and clear the calling
  * device's error word.  Returns CP_OK, CP_ETIMEOUT (a kernel's bounded wait
  * ran out and the kernel returned early; its outputs are undefined) or
