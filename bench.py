@@ -273,7 +273,46 @@ def extras(dev, stream, peaks):
             "time_max_over_mean": max(times) / (sum(times) / len(times)),
         }
     out["per_rank_long128k"] = per
+    del q, k, v, ob, lb_
+    # backward: B=2, H=16, S=32768, D=128, N=8, zigzag, causal
+    w = inputs.BWD32K
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    q, k, v, do = (torch.randn(w.B, w.S, w.Hq, w.D, device=dev, generator=g).to(torch.bfloat16)
+                   for _ in range(4))
+    o, l = api.ring_attn_fwd(q, k, v, w.N, w.layout, True, stream=stream)
+    ws = torch.empty(api.ring_attn_bwd_workspace(w.B, w.Hq, w.S), dtype=torch.uint8, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    fn = lambda: api.ring_attn_bwd(q, k, v, o, l, do, w.N, w.layout, True, dq=dq, dk=dk, dv=dv,
+                                   workspace=ws, stream=stream)
+    for _ in range(3):
+        fn()
+    ms = time_events(fn, 5, stream)
+    pairs = masked_pairs(w)
+    alg = 10 * w.D * w.B * w.Hq * pairs
+    out["ring_attn_bwd_bwd32k"] = {
+        "ms": ms, "flops_algorithmic": alg, "TFLOP/s": alg / ms / 1e9,
+        "frac_bf16_burst": alg / ms / 1e9 / peaks["bf16_tflops"],
+        "executed_TFLOP/s": 14 * w.D * w.B * w.Hq * pairs / ms / 1e9,
+        "note": "algorithmic 10*D FLOPs per masked-in pair; the kernels execute 14*D "
+                "(dQ recomputes S and dP instead of using atomics)"}
     return out
+
+
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x, world, device):
+    """Max of a per-rank float over all ranks (identity with one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_rank, world, ms_max):
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
 # ----------------------------------------------------------------------------- main
@@ -343,10 +382,7 @@ def main():
         if world > 1:
             dist.barrier()
         ms = e0.elapsed_time(e1) / args.steps
-        t = torch.tensor([ms], device=dev)
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item()), ms, clocks
+        return max_over_ranks(ms, world, dev), ms, clocks
 
     ms_max, ms_local, clocks = timed()
     remeasured = False
@@ -356,7 +392,7 @@ def main():
     assert api.cp_get_error() == 0
 
     flops = fwd_flops(w)
-    value = world * flops / (ms_max * 1e-3) / 1e12
+    value = job_value(flops, world, ms_max)
     achieved = flops / (ms_local * 1e-3) / 1e12
     long_run = args.steps * ms_local >= 1000.0
     peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
@@ -381,11 +417,7 @@ def main():
     e2e_steps = max(3, min(args.steps, 10))
     if world > 1:
         dist.barrier()
-    e2e_ms = time_events(e2e_step, e2e_steps, stream)
-    t = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(time_events(e2e_step, e2e_steps, stream), world, dev)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
 
@@ -404,7 +436,7 @@ def main():
                      "kernel": "fwd_bf16_kernel<128>",
                      "flops_per_launch": flops},
         "clocks": clocks,
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps,
     }

@@ -10,8 +10,8 @@
 //
 // The unit of copying is a run of H/N heads x D elements, contiguous on both
 // sides.  Runs are numbered in the order of the side that is read, so reads
-// are fully sequential; each thread moves one vector (16 bytes when sizes and
-// pointers allow) per iteration.  HBM-bound: bytes moved = 2 x tensor bytes.
+// are fully sequential; each thread moves four vectors (16 bytes when sizes
+// and pointers allow) per iteration, loads before stores.  HBM-bound: bytes moved = 2 x tensor bytes.
 #include <cuda_runtime.h>
 
 #include "cp_common.cuh"
@@ -38,51 +38,76 @@ __device__ __forceinline__ void locate(const Geom &g, int s, int &r, int &t)
     t = (g.layout == CP_LAYOUT_ZIGZAG && ch >= g.N) ? g.clen + within : within;
 }
 
-template <typename V, bool TO_HEAD>
+// Destination run of source run `run` (I: 32- or 64-bit index arithmetic).
+template <bool TO_HEAD, typename I>
+__device__ __forceinline__ I dest_run(const UlyArgs &u, I run)
+{
+    const I N = (I)u.g.N, B = (I)u.B, L = (I)u.L, S = (I)u.g.S;
+    if (TO_HEAD) {
+        // read side x: run = ((r*B + b)*L + t)*N + g
+        const I gi = run % N;
+        I rest = run / N;
+        const I t = rest % L;
+        rest /= L;
+        const I b = rest % B;
+        const I r = rest / B;
+        const I s = (I)shard_pos(u.g, (int)r, (int)t);
+        return (gi * B + b) * S + s;
+    }
+    // read side y: run = (g*B + b)*S + s
+    const I s = run % S;
+    I rest = run / S;
+    const I b = rest % B;
+    const I gi = rest / B;
+    int r, t;
+    locate(u.g, (int)s, r, t);
+    return (((I)r * B + b) * L + (I)t) * N + gi;
+}
+
+// Each thread moves UNROLL vectors, blockDim apart (coalesced), with all loads
+// issued before the stores so that several requests per thread are in flight.
+template <typename V, bool TO_HEAD, typename I>
 __global__ void __launch_bounds__(256) ulysses_kernel(const V *__restrict__ src, V *__restrict__ dst,
                                                       UlyArgs u)
 {
-    const int N = u.g.N;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < u.total; v += stride) {
-        const int64_t run = v / u.run_vecs;
-        const int64_t e = v - run * u.run_vecs;
-        int64_t other;
-        if (TO_HEAD) {
-            // read side x: run = ((r*B + b)*L + t)*N + g
-            const int gi = (int)(run % N);
-            int64_t rest = run / N;
-            const int t = (int)(rest % u.L);
-            rest /= u.L;
-            const int b = (int)(rest % u.B);
-            const int r = (int)(rest / u.B);
-            const int s = shard_pos(u.g, r, t);
-            other = (((int64_t)gi * u.B + b) * u.g.S + s);
-        } else {
-            // read side y: run = (g*B + b)*S + s
-            const int s = (int)(run % u.g.S);
-            int64_t rest = run / u.g.S;
-            const int b = (int)(rest % u.B);
-            const int gi = (int)(rest / u.B);
-            int r, t;
-            locate(u.g, s, r, t);
-            other = ((((int64_t)r * u.B + b) * u.L + t) * N + gi);
+    constexpr int UNROLL = 4;
+    const I total = (I)u.total, rv = (I)u.run_vecs;
+    const I step = (I)gridDim.x * blockDim.x * UNROLL;
+    for (I v0 = (I)blockIdx.x * blockDim.x * UNROLL + threadIdx.x; v0 < total; v0 += step) {
+        V val[UNROLL];
+#pragma unroll
+        for (int i = 0; i < UNROLL; ++i) {
+            const I v = v0 + (I)i * blockDim.x;
+            if (v < total) val[i] = src[v];
         }
-        dst[other * u.run_vecs + e] = src[v];
+#pragma unroll
+        for (int i = 0; i < UNROLL; ++i) {
+            const I v = v0 + (I)i * blockDim.x;
+            if (v < total) {
+                const I run = v / rv;
+                dst[dest_run<TO_HEAD, I>(u, run) * rv + (v - run * rv)] = val[i];
+            }
+        }
     }
 }
 
 template <typename V>
 int launch_v(const void *src, void *dst, const UlyArgs &u, int to_head, cudaStream_t st)
 {
-    int64_t blocks = (u.total + 255) / 256;
+    int64_t blocks = (u.total + 1023) / 1024;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return CP_OK;
-    if (to_head)
-        ulysses_kernel<V, true><<<(unsigned)blocks, 256, 0, st>>>((const V *)src, (V *)dst, u);
-    else
-        ulysses_kernel<V, false><<<(unsigned)blocks, 256, 0, st>>>((const V *)src, (V *)dst, u);
+    const bool small = u.total < 0x7fffffffLL && (int64_t)u.B * u.g.S * u.g.N < 0x7fffffffLL;
+    const V *s = (const V *)src;
+    V *d = (V *)dst;
+    if (small) {
+        if (to_head) ulysses_kernel<V, true, uint32_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+        else ulysses_kernel<V, false, uint32_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+    } else {
+        if (to_head) ulysses_kernel<V, true, int64_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+        else ulysses_kernel<V, false, int64_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+    }
     return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
 }
 
