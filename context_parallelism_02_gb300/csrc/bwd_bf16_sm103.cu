@@ -58,6 +58,35 @@ struct Tile {
     static constexpr int BYTES = BOXES * BOX;
 };
 
+// Unrolled issue sequences (compile-time offsets added to base descriptors
+// inside the MMA asm): the MMA thread shares its SM sub-partition with busy
+// gradient warps, so it must spend as few instructions per MMA as possible.
+
+// D/16 MMAs M=128, N=128, K=16, A and B K-major (128-row boxes of 16 KB)
+template <int KK, int D>
+__device__ __forceinline__ void ss_seq(uint32_t tD, uint64_t dA, uint64_t dB, uint32_t id)
+{
+    if constexpr (KK < D / 16) {
+        constexpr uint32_t o = (uint32_t)(((KK >> 2) * 16384 + (KK & 3) * 32) >> 4);
+        mma_ss_off<o, o>(tD, dA, dB, id, KK > 0 ? 1u : 0u);
+        ss_seq<KK + 1, D>(tD, dA, dB, id);
+    }
+}
+
+// 8 MMAs M=128, N=D, K=16: A (bf16 pairs) from tensor-memory columns
+// [0,32) and [64,96) relative to tA, B MN-major; acc0 = accumulate flag of the first
+template <int KK>
+__device__ __forceinline__ void ts_seq(uint32_t tD, uint32_t tA, uint64_t dB, uint32_t id,
+                                       uint32_t acc0)
+{
+    if constexpr (KK < T / 16) {
+        constexpr uint32_t acol = (KK < 4) ? (uint32_t)(KK * 8) : (uint32_t)(64 + (KK - 4) * 8);
+        constexpr uint32_t ob = (uint32_t)((KK * 16 * 128) >> 4);
+        mma_ts_off<ob>(tD, tA + acol, dB, id, KK == 0 ? acc0 : 1u);
+        ts_seq<KK + 1>(tD, tA, dB, id, acc0);
+    }
+}
+
 // ----------------------------------------------------------------------------- Delta
 
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__restrict__ out,
@@ -168,7 +197,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(BAR(Q_VEMPTY + i), 1);
         }
         mbar_init(BAR(Q_SDP), 1);
-        mbar_init(BAR(Q_DS), 256);
+        mbar_init(BAR(Q_DS), 8);
         mbar_init(BAR(Q_FIN), 1);
         mbar_init(BAR(Q_DRAIN), 1);
         *abort_flag = 0;
@@ -226,19 +255,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t idSP = idesc_bf16(128, T, false);      // S, dP: K-major A and B
             constexpr uint32_t idDQ = idesc_bf16(128, D, true);       // dQ: B = K MN-major
             const uint32_t tS = tmem, tP = tmem + 128u, tQ = tmem + 256u;
+            const uint64_t dQd = sdesc(sQ, 16, 1024), dDOd = sdesc(sDO, 16, 1024);
+            const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, 16, 1024);
+            const uint64_t dKmn0 = sdesc(sK, 16384, 1024);
             auto issue_sdp = [&](int st) {
-#pragma unroll 1
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-                    mma_ss(tS, sdesc(sQ + off, 16, 1024), sdesc(sK + st * TB + off, 16, 1024), idSP,
-                           kk > 0);
-                }
-#pragma unroll 1
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-                    mma_ss(tP, sdesc(sDO + off, 16, 1024), sdesc(sV + st * TB + off, 16, 1024), idSP,
-                           kk > 0);
-                }
+                const uint64_t so = (uint64_t)(st * (TB >> 4));
+                ss_seq<0, D>(tS, dQd, dK0 + so, idSP);
+                ss_seq<0, D>(tP, dDOd, dV0 + so, idSP);
             };
             bool ok = wait1(BAR(Q_QFULL), 0, wc) && wait1(BAR(Q_KFULL), 0, wc) && wait1(BAR(Q_VFULL), 0, wc);
             if (ok) {
@@ -252,12 +275,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!wait1(BAR(Q_DS), j & 1, wc)) break;
                 tc_fence_after();
                 // dQ += dS K_j; dS (bf16) sits in columns [0,32) and [64,96) of S
-#pragma unroll 1
-                for (int kk = 0; kk < T / 16; ++kk) {
-                    const uint32_t acol = (kk < 4) ? (uint32_t)(kk * 8) : (uint32_t)(64 + (kk - 4) * 8);
-                    mma_ts(tQ, tS + acol, sdesc(sK + st * TB + kk * 16 * 128, 16384, 1024), idDQ,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                ts_seq<0>(tQ, tS, dKmn0 + (uint64_t)(st * (TB >> 4)), idDQ, j > 0 ? 1u : 0u);
                 mma_commit(BAR(Q_KEMPTY + st));
                 if (j + 1 < n) {
                     const int sn = (j + 1) & 1;
@@ -335,7 +353,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_st_x32(tS, pk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(Q_DS));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_DS));
         }
         if (ok && waitw(BAR(Q_FIN), 0, wc)) {
             tc_fence_after();
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(BAR(K_QEMPTY + i), 1);
         }
         mbar_init(BAR(K_SDP), 1);
-        mbar_init(BAR(K_PDS), 256);
+        mbar_init(BAR(K_PDS), 8);
         mbar_init(BAR(K_FIN), 1);
         mbar_init(BAR(K_DRAIN), 1);
         *abort_flag = 0;
@@ -502,31 +521,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t idSP = idesc_bf16(128, T, false);    // S^T, dP^T
             constexpr uint32_t idKV = idesc_bf16(128, D, true);     // dV, dK: B MN-major
             const uint32_t tS = tmem, tP = tmem + 128u, tV = tmem + 256u, tK = tmem + 384u;
+            const uint64_t dKd = sdesc(sK, 16, 1024), dVd = sdesc(sV, 16, 1024);
+            const uint64_t dQ0 = sdesc(sQ, 16, 1024), dDO0 = sdesc(sDO, 16, 1024);
+            const uint64_t dQmn0 = sdesc(sQ, 16384, 1024), dDOmn0 = sdesc(sDO, 16384, 1024);
             bool ok = wait1(BAR(K_KVFULL), 0, wc);
             for (int i = 0; ok && i < n; ++i) {
                 const int st = i & 1;
                 if (!wait1(BAR(K_QFULL + st), (i >> 1) & 1, wc)) break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-                    mma_ss(tS, sdesc(sK + off, 16, 1024), sdesc(sQ + st * TB + off, 16, 1024), idSP, kk > 0);
-                }
-#pragma unroll 1
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-                    mma_ss(tP, sdesc(sV + off, 16, 1024), sdesc(sDO + st * TB + off, 16, 1024), idSP, kk > 0);
-                }
+                const uint64_t so = (uint64_t)(st * (TB >> 4));
+                ss_seq<0, D>(tS, dKd, dQ0 + so, idSP);
+                ss_seq<0, D>(tP, dVd, dDO0 + so, idSP);
                 mma_commit(BAR(K_SDP));
                 if (!wait1(BAR(K_PDS), i & 1, wc)) break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int kk = 0; kk < T / 16; ++kk) {
-                    const uint32_t acol = (kk < 4) ? (uint32_t)(kk * 8) : (uint32_t)(64 + (kk - 4) * 8);
-                    const uint32_t boff = (uint32_t)(kk * 16 * 128);
-                    mma_ts(tV, tS + acol, sdesc(sDO + st * TB + boff, 16384, 1024), idKV, (i > 0 || kk > 0));
-                    mma_ts(tK, tP + acol, sdesc(sQ + st * TB + boff, 16384, 1024), idKV, (i > 0 || kk > 0));
-                }
+                ts_seq<0>(tV, tS, dDOmn0 + (uint64_t)(st * (TB >> 4)), idKV, i > 0 ? 1u : 0u);
+                ts_seq<0>(tK, tP, dQmn0 + (uint64_t)(st * (TB >> 4)), idKV, i > 0 ? 1u : 0u);
                 mma_commit(BAR(K_QEMPTY + st));
             }
             mma_commit(BAR(K_FIN));
@@ -590,7 +600,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_st_x32(tP, dd);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(K_PDS));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(K_PDS));
         }
         if (ok && waitw(BAR(K_FIN), 0, wc)) {
             tc_fence_after();

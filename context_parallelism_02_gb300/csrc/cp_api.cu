@@ -152,9 +152,9 @@ int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_h
         if (tiles_host) tiles_host[i] = 0;
     }
     if (S == 0) return CP_OK;
-    // Walk the units and KV tiles of the bf16 kernel (two 128-row query tiles
-    // per unit, 128-key KV tiles) and count what each query tile covers.
-    constexpr int QROWS = 256, T = 128;
+    // Walk the units and KV tiles of the bf16 kernel (one 128-row query tile
+    // per unit, 256-key KV tiles) and count what each query tile covers.
+    constexpr int QROWS = 128, T = 256;
     const Geom g = make_geom((int)S, N, layout, causal);
     const int upc = (g.clen + QROWS - 1) / QROWS;
     const int units = num_selected_chunks(g, 0, N) * upc;
@@ -164,9 +164,9 @@ int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_h
         it.begin(g, w.r, w.qmax);
         for (; it.valid(); it.next()) {
             const int64_t ks = it.start(), ke = ks + it.len();   // keys [ks, ke)
-            for (int qi = 0; qi < 2; ++qi) {
-                const int64_t qa = w.q0 + (int64_t)qi * T;
-                int64_t qb = qa + T;                           // queries [qa, qb)
+            for (int qi = 0; qi < QROWS / 128; ++qi) {
+                const int64_t qa = w.q0 + (int64_t)qi * 128;
+                int64_t qb = qa + 128;                         // queries [qa, qb)
                 if (qb > w.cend) qb = w.cend;
                 if (qa >= qb) continue;
                 const int64_t p = causal ? visible_pairs(qa, qb, ks, ke - ks) : (qb - qa) * (ke - ks);

@@ -11,29 +11,29 @@
 // SM: O lives in tensor memory from the first KV tile of step 0 to the last
 // tile of step N-1.
 //
-// Work unit: two 128-row query tiles (Q0, Q1) of one chunk and one
-// (batch, query head); both share every K/V tile.  Units are launched in
-// descending query position, which under a causal mask is descending work.
+// Work unit: one 128-row query tile of one chunk and one (batch, query head),
+// walking 256-key tiles.  S = Q K^T is issued as M=128, N=256 MMAs: on this
+// part an N=128 MMA pays a fixed overhead (about 90 cycles for 64 cycles of
+// work) that an N=256 one hides.  Units are launched in descending query
+// position, which under a causal mask is descending work.
 //
 // Roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: Q0/Q1 once, then K_j and V_j into 2-deep rings;
-//               also allocates / frees the 512 tensor-memory columns.
-//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T (SS, both K-major,
-//               128B-swizzled) and O_i += P_i V_j (P from tensor memory, V
-//               MN-major), commits to mbarriers.
-//   warps 2-3   idle (they only complete warpgroup 0)
-//   warps 4-7   softmax of Q0, warps 8-11 softmax of Q1: one thread per query
-//               row, reads its S row from tensor memory, masks partial tiles,
-//               keeps (m, l), writes P (bf16) back over S, rescales its O row
-//               only when the running max grew by more than 2^8, and writes
-//               out / lse at the end.
-// Issue order of the MMA thread per KV tile j:
-//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
-// so a completed S_i(j+1) also guarantees PV_i(j) finished: the softmax warps
-// may then rescale O_i and overwrite P_i without another barrier.
-//
-// Tensor memory columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D),
-// O1 [384,384+D).
+//   warp 0      TMA producer: Q once; K tiles (256 rows) into a 2-deep ring
+//               one tile ahead; V tiles as two 128-row halves; also allocates
+//               and frees the 512 tensor-memory columns.
+//   warp 1      MMA issuer (one thread).
+//   warps 2-3   idle (they complete warpgroup 0 for the register split).
+//   warps 4-7   softmax of key columns [0,128), warps 8-11 of [128,256):
+//               one thread per query row.  The halves exchange row maxima
+//               through shared memory (an mbarrier per tile, bounded wait),
+//               so both keep the same running max.
+// Tensor memory columns: S [0,256) fp32, P [256,384) bf16 pairs,
+// O [384,384+D) fp32.  P has its own columns, so the issue order per tile
+//   S(j+1)  (as soon as the softmax has read S(j)),  PV(j)  (once P(j) is written)
+// keeps the tensor pipe busy while the softmax computes exponentials.  The
+// softmax writes P(j+1) and rescales O only after the commit of PV(j).  O is
+// rescaled only when the running max grows by more than 2^8 (exact: the same
+// stale max is used for P and l).
 //
 // Every wait is bounded (cp_common.cuh); on time-out the block records
 // CP_ETIMEOUT, drains its copies and MMAs, frees tensor memory and exits.
@@ -52,47 +52,77 @@ namespace {
 
 using namespace tc;
 
-constexpr int QT = 128;          // query rows per tile
-constexpr int KT = 128;          // keys per KV tile
-constexpr int KST = 2;           // K ring depth
-constexpr int VST = 2;           // V ring depth
+constexpr int QT = 128;          // query rows per unit
+constexpr int KT = 256;          // keys per KV tile
 constexpr int NTHREADS = 384;
 // Register split (setmaxnreg): the block launches at 168 registers per thread
-// (64512 in total); warpgroup 0 (producer, MMA issuer, two idle warps) drops to
-// 56 and the two softmax warpgroups rise to 208: 128*56 + 256*208 = 60416.
+// (64512 in total); warpgroup 0 drops to 56 and the two softmax warpgroups
+// rise to 208: 128*56 + 256*208 = 60416.
 constexpr int REGS_CTRL = 56;
 constexpr int REGS_SOFTMAX = 208;
-static_assert(true, "");
+static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= NTHREADS * 168, "register split exceeds the launch budget");
 constexpr float RESCALE_LOG2 = 8.0f;   // rescale O only when the max grows by > 2^8
 
 enum {
     B_Q = 0,
-    B_KFULL = 1,
-    B_KEMPTY = B_KFULL + KST,
-    B_VFULL = B_KEMPTY + KST,
-    B_VEMPTY = B_VFULL + VST,
-    B_SFULL = B_VEMPTY + VST,
-    B_PFULL = B_SFULL + 2,
-    B_OFIN = B_PFULL + 2,
-    B_DRAIN = B_OFIN + 2,
-    NBAR = B_DRAIN + 1
+    B_KFULL = 1,     // 2 K stages
+    B_KEMPTY = 3,
+    B_VFULL = 5,     // 2 V halves
+    B_VEMPTY = 7,
+    B_SFULL = 9,
+    B_SFREE = 10,    // one arrival per softmax warp (8): S(j) read
+    B_PFULL = 11,    // one arrival per softmax warp (8): P(j) written
+    B_PFREE = 12,    // PV(j) complete
+    B_OFIN = 13,
+    B_DRAIN = 14,
+    B_MX = 15,       // one arrival per softmax warp (8): row maxima / sums published
+    NBAR = 16
 };
 
 template <int D>
 struct Cfg {
-    static constexpr int BOXES = D / 64;        // 64-element (128-byte) column boxes per tile
-    static constexpr int BOX = 128 * 128;       // bytes of one box: 128 rows x 128 bytes
-    static constexpr int TILE = BOXES * BOX;    // bytes of one 128-row bf16 tile
+    static constexpr int QBYTES = QT * D * 2;          // Q tile: D/64 boxes of 128 rows
+    static constexpr int KBYTES = KT * D * 2;          // K stage: D/64 boxes of 256 rows
+    static constexpr int KBOX = KT * 128;              // bytes of one 256-row box
+    static constexpr int VBYTES = 128 * D * 2;         // V half: D/64 boxes of 128 rows
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + 2 * TILE;
-    static constexpr int OFF_V = OFF_K + KST * TILE;
-    static constexpr int OFF_BAR = OFF_V + VST * TILE;
+    static constexpr int OFF_K = OFF_Q + QBYTES;
+    static constexpr int OFF_V = OFF_K + 2 * KBYTES;
+    static constexpr int OFF_PM = OFF_V + 2 * VBYTES;  // row-max exchange: [2][2][128] fp32
+    static constexpr int OFF_BAR = OFF_PM + 2 * 2 * 128 * 4;
     static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
-    // + slack to align the base to 1 KB; at least 120 KB so that one block
-    // owns the SM and its 512 tensor-memory columns
-    static constexpr int SMEM_NEED = OFF_MISC + 16 + 1024;
+    static constexpr int SMEM_NEED = OFF_MISC + 16;
+    // at least 120 KB so that one block owns the SM and its 512 TMEM columns
     static constexpr int SMEM = SMEM_NEED > 120 * 1024 ? SMEM_NEED : 120 * 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
 };
+
+// --- unrolled issue sequences -----------------------------------------------------
+
+// S = Q K^T: D/16 MMAs of M=128, N=256, K=16 (both operands K-major, 128B swizzle)
+template <int KK, int D>
+__device__ __forceinline__ void issue_s_seq(uint32_t tS, uint64_t dQ, uint64_t dK, uint32_t id)
+{
+    if constexpr (KK < D / 16) {
+        constexpr uint32_t oq = (uint32_t)(((KK >> 2) * 16384 + (KK & 3) * 32) >> 4);
+        constexpr uint32_t ok = (uint32_t)(((KK >> 2) * Cfg<D>::KBOX + (KK & 3) * 32) >> 4);
+        mma_ss_off<oq, ok>(tS, dQ, dK, id, KK > 0 ? 1u : 0u);
+        issue_s_seq<KK + 1, D>(tS, dQ, dK, id);
+    }
+}
+
+// O += P V for one 128-key half: 8 MMAs of M=128, N=D, K=16 (P from tensor
+// memory, V MN-major).  acc0 is the accumulate flag of the first one.
+template <int K8, int HH>
+__device__ __forceinline__ void issue_pv_seq(uint32_t tO, uint32_t tP, uint64_t dV, uint32_t id,
+                                             uint32_t acc0)
+{
+    if constexpr (K8 < 8) {
+        constexpr uint32_t ov = (uint32_t)((K8 * 16 * 128) >> 4);
+        mma_ts_off<ov>(tO, tP + (uint32_t)((8 * HH + K8) * 8), dV, id, K8 == 0 ? acc0 : 1u);
+        issue_pv_seq<K8 + 1, HH>(tO, tP, dV, id, acc0);
+    }
+}
 
 // --- the kernel ------------------------------------------------------------------
 
@@ -103,11 +133,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     __nv_bfloat16 *__restrict__ out, float *__restrict__ lse)
 {
     using C = Cfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_u32(smem_raw);
+    if (base & 1023u) {   // the 128B-swizzled tiles need 1 KB alignment
+        if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_TIMEOUT);
+        return;
+    }
+    uint8_t *gbase = smem_raw;
     const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+    float *pm = reinterpret_cast<float *>(gbase + C::OFF_PM);
     const uint32_t bar0 = base + C::OFF_BAR;
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
@@ -115,26 +149,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
-    const Unit w = decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, 2 * QT, blockIdx.x);
+    const Unit w = decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, blockIdx.x);
     const int kvh = w.h / (a.Hq / a.Hkv);
     const int n = KvIter<KT>::count(g, w.r, w.qmax);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_Q), 1);
-        for (int i = 0; i < KST; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(B_KFULL + i), 1);
             mbar_init(BAR(B_KEMPTY + i), 1);
-        }
-        for (int i = 0; i < VST; ++i) {
             mbar_init(BAR(B_VFULL + i), 1);
             mbar_init(BAR(B_VEMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(BAR(B_SFULL + i), 1);
-            mbar_init(BAR(B_PFULL + i), 128);
-            mbar_init(BAR(B_OFIN + i), 1);
-        }
+        mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_SFREE), 8);
+        mbar_init(BAR(B_PFULL), 8);
+        mbar_init(BAR(B_PFREE), 1);
+        mbar_init(BAR(B_OFIN), 1);
         mbar_init(BAR(B_DRAIN), 1);
+        mbar_init(BAR(B_MX), 8);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -152,114 +185,111 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
-        if (warp == 0) {
+        if (warp == 0 && lane == 0) {
             // ------------------------------------------------------------ producer
-            if (lane == 0) {
-                const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
-                mbar_arrive_expect_tx(BAR(B_Q), 2 * C::TILE);
-                for (int qi = 0; qi < 2; ++qi)
-                    for (int bx = 0; bx < C::BOXES; ++bx)
-                        tma_load4(sQ + qi * C::TILE + bx * C::BOX, &tmQ, BAR(B_Q), bx * 64, w.h,
-                                  w.q0 + qi * QT, w.b, pol_q);
-                KvIter<KT> it;
-                it.begin(g, w.r, w.qmax);
-                int issued = 0;
-                for (int j = 0; j < n; ++j, it.next()) {
-                    const int sk = j % KST, sv = j % VST;
-                    const int row = it.start();
-                    if (j >= KST && !wait1(BAR(B_KEMPTY + sk), ((j / KST) - 1) & 1, wc)) break;
-                    mbar_arrive_expect_tx(BAR(B_KFULL + sk), C::TILE);
-                    for (int bx = 0; bx < C::BOXES; ++bx)
-                        tma_load4(sK + sk * C::TILE + bx * C::BOX, &tmK, BAR(B_KFULL + sk), bx * 64,
-                                  kvh, row, w.b, pol_kv);
-                    if (j >= VST && !wait1(BAR(B_VEMPTY + sv), ((j / VST) - 1) & 1, wc)) {
-                        issued = -(j + 1);   // K_j issued, V_j not
+            const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+            mbar_arrive_expect_tx(BAR(B_Q), C::QBYTES);
+            for (int bx = 0; bx < D / 64; ++bx)
+                tma_load4(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, w.h, w.q0, w.b, pol_q);
+            // K runs one tile ahead of V; the V loads reuse the K tile starts
+            KvIter<KT> itk;
+            itk.begin(g, w.r, w.qmax);
+            int nk = 0, nv = 0;   // tiles whose K / V loads were issued
+            int ks_cur = 0, ks_next = 0;
+            bool ok = true;
+            auto load_k = [&](int j) -> bool {
+                const int st = j & 1;
+                if (j >= 2 && !wait1(BAR(B_KEMPTY + st), ((j >> 1) - 1) & 1, wc)) return false;
+                mbar_arrive_expect_tx(BAR(B_KFULL + st), C::KBYTES);
+                ks_next = itk.start();
+                for (int bx = 0; bx < D / 64; ++bx)
+                    tma_load4(sK + st * C::KBYTES + bx * C::KBOX, &tmK, BAR(B_KFULL + st), bx * 64,
+                              kvh, ks_next, w.b, pol_kv);
+                itk.next();
+                ++nk;
+                return true;
+            };
+            if (n > 0) ok = load_k(0);
+            for (int j = 0; ok && j < n; ++j) {
+                ks_cur = ks_next;
+                if (j + 1 < n && !load_k(j + 1)) break;
+                const int ks = ks_cur;
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (j >= 1 && !wait1(BAR(B_VEMPTY + hh), (j - 1) & 1, wc)) {
+                        ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(BAR(B_VFULL + sv), C::TILE);
-                    for (int bx = 0; bx < C::BOXES; ++bx)
-                        tma_load4(sV + sv * C::TILE + bx * C::BOX, &tmV, BAR(B_VFULL + sv), bx * 64,
-                                  kvh, row, w.b, pol_kv);
-                    issued = j + 1;
-                }
-                // Drain: wait (bounded) for the copies still in flight so none lands
-                // after the block exits.  In a normal run these have all completed.
-                if (*abort_flag) {
-                    const int nk = issued < 0 ? -issued : issued;
-                    const int nv = issued < 0 ? -issued - 1 : issued;
-                    WaitCtl dc{a.err, abort_flag, a.limit_ns};
-                    volatile int no_abort = 0;
-                    dc.abort = &no_abort;
-                    mbar_try_wait(BAR(B_Q), 0) || wait1(BAR(B_Q), 0, dc);
-                    for (int j = (nk > KST ? nk - KST : 0); j < nk; ++j)
-                        wait1(BAR(B_KFULL + j % KST), (j / KST) & 1, dc);
-                    for (int j = (nv > VST ? nv - VST : 0); j < nv; ++j)
-                        wait1(BAR(B_VFULL + j % VST), (j / VST) & 1, dc);
+                    mbar_arrive_expect_tx(BAR(B_VFULL + hh), C::VBYTES);
+                    for (int bx = 0; bx < D / 64; ++bx)
+                        tma_load4(sV + hh * C::VBYTES + bx * 16384, &tmV, BAR(B_VFULL + hh), bx * 64,
+                                  kvh, ks + 128 * hh, w.b, pol_kv);
+                    nv = 2 * j + hh + 1;
                 }
             }
-        } else if (warp == 1) {
-            // ------------------------------------------------------------ MMA issuer
-            if (lane == 0) {
-                constexpr uint32_t idS = idesc_bf16(128, KT, false);
-                constexpr uint32_t idO = idesc_bf16(128, D, true);
-                // S_i / P_i at columns 128*i, O_i at 256 + 128*i
-                auto issue_S = [&](int qi, int sk) {
-                    const uint32_t tS = tmem + 128u * qi;
-    #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (uint32_t)((kk >> 2) * C::BOX + (kk & 3) * 32);
-                        const uint64_t ad = sdesc(sQ + qi * C::TILE + off, 16, 1024);
-                        const uint64_t bd = sdesc(sK + sk * C::TILE + off, 16, 1024);
-                        mma_ss(tS, ad, bd, idS, kk > 0 ? 1u : 0u);
-                    }
-                };
-                auto issue_PV = [&](int qi, int sv, bool acc) {
-                    const uint32_t tS = tmem + 128u * qi, tO = tmem + 256u + 128u * qi;
-    #pragma unroll
-                    for (int kk = 0; kk < KT / 16; ++kk) {
-                        const uint64_t bd = sdesc(sV + sv * C::TILE + kk * 16 * 128, C::BOX, 1024);
-                        mma_ts(tO, tS + (uint32_t)(kk * 8), bd, idO, (acc || kk > 0) ? 1u : 0u);
-                    }
-                };
-                bool ok = wait1(BAR(B_Q), 0, wc) && wait1(BAR(B_KFULL + 0), 0, wc);
-                if (ok) {
-                    tc_fence_after();
-                    issue_S(0, 0);
-                    mma_commit(BAR(B_SFULL + 0));
-                    issue_S(1, 0);
-                    mma_commit(BAR(B_SFULL + 1));
-                    mma_commit(BAR(B_KEMPTY + 0));
-                }
-                for (int j = 0; ok && j < n; ++j) {
-                    const int sv = j % VST;
-                    const bool has_next = (j + 1) < n;
-                    const int sk = (j + 1) % KST;
-                    if (!wait1(BAR(B_VFULL + sv), (j / VST) & 1, wc)) break;
-                    if (has_next && !wait1(BAR(B_KFULL + sk), ((j + 1) / KST) & 1, wc)) break;
-                    for (int qi = 0; qi < 2; ++qi) {
-                        if (!wait1(BAR(B_PFULL + qi), j & 1, wc)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_PV(qi, sv, j > 0);
-                        if (qi == 1) mma_commit(BAR(B_VEMPTY + sv));
-                        if (has_next) {
-                            issue_S(qi, sk);
-                            mma_commit(BAR(B_SFULL + qi));
-                            if (qi == 1) mma_commit(BAR(B_KEMPTY + sk));
-                        } else {
-                            mma_commit(BAR(B_OFIN + qi));
-                        }
-                    }
-                }
-                // all MMAs of this block are complete once the drain barrier fires
-                mma_commit(BAR(B_DRAIN));
-                WaitCtl dc{a.err, abort_flag, a.limit_ns};
+            if (*abort_flag) {
+                // Drain: wait (bounded) for the copies still in flight.
                 volatile int no_abort = 0;
-                dc.abort = &no_abort;
-                wait1(BAR(B_DRAIN), 0, dc);
+                WaitCtl dc{a.err, &no_abort, a.limit_ns};
+                wait1(BAR(B_Q), 0, dc);
+                for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(B_KFULL + (j & 1)), (j >> 1) & 1, dc);
+                for (int x = nv > 2 ? nv - 2 : 0; x < nv; ++x) wait1(BAR(B_VFULL + (x & 1)), (x >> 1) & 1, dc);
             }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            constexpr uint32_t idS = idesc_bf16(128, KT, false);
+            constexpr uint32_t idO = idesc_bf16(128, D, true);
+            const uint32_t tS = tmem, tP = tmem + 256u, tO = tmem + 384u;
+            // The MMA thread shares its SM sub-partition with two busy softmax
+            // warps, so every instruction it spends between MMAs delays the
+            // tensor pipe: descriptors are built once per buffer and the issue
+            // sequences are unrolled at compile time (offsets are immediates).
+            const uint64_t dQ = sdesc(sQ, 16, 1024);
+            const uint64_t dK0 = sdesc(sK, 16, 1024);
+            const uint64_t dV0 = sdesc(sV, 16384, 1024);
+            auto issue_S = [&](int st) {
+                issue_s_seq<0, D>(tS, dQ, dK0 + (uint64_t)(st * (C::KBYTES >> 4)), idS);
+            };
+            bool ok = n > 0 && wait1(BAR(B_Q), 0, wc) && wait1(BAR(B_KFULL), 0, wc);
+            if (ok) {
+                tc_fence_after();
+                issue_S(0);
+                mma_commit(BAR(B_SFULL));
+                mma_commit(BAR(B_KEMPTY));
+            }
+            for (int j = 0; ok && j < n; ++j) {
+                if (j + 1 < n) {
+                    const int st = (j + 1) & 1;
+                    if (!wait1(BAR(B_SFREE), j & 1, wc) ||
+                        !wait1(BAR(B_KFULL + st), ((j + 1) >> 1) & 1, wc))
+                        break;
+                    tc_fence_after();
+                    issue_S(st);
+                    mma_commit(BAR(B_SFULL));
+                    mma_commit(BAR(B_KEMPTY + st));
+                }
+                if (!wait1(BAR(B_PFULL), j & 1, wc)) break;
+                tc_fence_after();
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!wait1(BAR(B_VFULL + hh), j & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (hh == 0)
+                        issue_pv_seq<0, 0>(tO, tP, dV0, idO, j > 0 ? 1u : 0u);
+                    else
+                        issue_pv_seq<0, 1>(tO, tP, dV0 + (uint64_t)(C::VBYTES >> 4), idO, 1u);
+                    mma_commit(BAR(B_VEMPTY + hh));
+                }
+                if (!ok) break;
+                mma_commit(BAR(B_PFREE));
+                if (j + 1 == n) mma_commit(BAR(B_OFIN));
+            }
+            // all MMAs of this block are complete once the drain barrier fires
+            mma_commit(BAR(B_DRAIN));
+            volatile int no_abort = 0;
+            WaitCtl dc{a.err, &no_abort, a.limit_ns};
+            wait1(BAR(B_DRAIN), 0, dc);
         }
         // end of warpgroup 0: wait for every role, then warp 0 frees tensor memory
         __syncwarp();
@@ -273,98 +303,159 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
         // ------------------------------------------------------------ softmax
-        const int qi = (warp - 4) >> 2;
+        const int half = (warp - 4) >> 2;            // key columns [128*half, 128*half+128)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + (qi ? 128u : 0u);
-        const uint32_t tO = tmem + lane_off + (qi ? 384u : 256u);
-        const int qfirst = w.q0 + qi * QT;
-        const int qpos = qfirst + row;
+        const uint32_t tS = tmem + lane_off + 128u * half;
+        const uint32_t tP = tmem + lane_off + 256u + 64u * half;
+        const uint32_t tO = tmem + lane_off + 384u + (uint32_t)(D / 2) * half;
+        const int qpos = w.q0 + row;
         const float NEG_INF = -INFINITY;
-        float m_run = NEG_INF, l_run = 0.f;
+        float m_run = NEG_INF, l_run = 0.f;      // l_run: this half's share of the row sum
         bool ok = true;
 
         KvIter<KT> it;
         it.begin(g, w.r, w.qmax);
         for (int j = 0; j < n; ++j, it.next()) {
-            if (!waitw(BAR(B_SFULL + qi), j & 1, wc)) {
+            if (!waitw(BAR(B_SFULL), j & 1, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld_x128(tS, sr);
+            // S(j) may now be overwritten: one arrival per warp (per-thread
+            // arrivals would serialise 256 atomics on one shared-memory word)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SFREE));
             float *s = reinterpret_cast<float *>(sr);
             const int ks = it.start();
             const int kl = it.len();
-            if (kl < KT || (a.causal && ks + kl - 1 > qfirst)) {
-                // partial tile: columns [0, lim) are visible to this row
+            if (kl < KT || (a.causal && ks + kl - 1 > w.q0)) {
+                // partial tile: key columns [0, lim) of the 256 are visible to this row
                 int lim = kl;
                 if (a.causal) {
                     const int c = qpos - ks + 1;
                     lim = c < lim ? c : lim;
                 }
+                lim -= 128 * half;
 #pragma unroll
-                for (int c = 0; c < KT; ++c)
+                for (int c = 0; c < 128; ++c)
                     if (c >= lim) s[c] = NEG_INF;
             }
+            // row max over this half: four independent 3-input max chains
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-            for (int c = 4; c < KT; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
+            for (int c = 4; c < 124; c += 8) {
+                mx0 = fmax3(mx0, s[c], s[c + 1]);
+                mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
             }
-            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-            const float mn = fmaxf(m_run, mt);
-            const bool need = mn > m_run + RESCALE_LOG2;
-            if (__any_sync(0xffffffffu, need)) {
-                const float f = need ? ex2(m_run - mn) : 1.f;
-                if (j > 0) {
-                    // O_i holds PV_i(0..j-1) (complete: S_i(j) was committed after it)
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld_x32(tO + 32u * c, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                        tmem_st_x32(tO + 32u * c, o);
-                    }
+            mx0 = fmax3(mx0, s[124], s[125]);
+            mx1 = fmax3(mx1, s[126], s[127]);
+            mx0 = fmax3(mx0, mx2, mx3);
+            // Publish this half's row maximum (double-buffered by tile parity; the
+            // barrier's phase j completes once all 256 threads published theirs).
+            float *pmj = pm + (j & 1) * 256;
+            const float mloc = fmaxf(mx0, mx1) * sl2;
+            pmj[half * 128 + row] = fmaxf(mx0, mx1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_MX));
+            // The exponentials use the running max m_run as long as this half's own
+            // maximum stays within 2^8 of it (P <= 2^8, no overflow), so the exchange
+            // is off the critical path; the combined max is checked afterwards and,
+            // in the rare case it grew by more than 2^8, P is scaled down to the new
+            // max.  The first visible tile (m_run = -inf) and a half whose own max
+            // jumped take the exchanged max first.
+            const bool early = __any_sync(0xffffffffu, mloc > m_run + RESCALE_LOG2);
+            float mt = NEG_INF;
+            if (early) {
+                if (!waitw(BAR(B_MX), j & 1, wc)) {
+                    ok = false;
+                    break;
                 }
-                if (need) {
-                    l_run *= f;
-                    m_run = mn;
-                }
+                mt = fmaxf(pmj[0 * 128 + row], pmj[1 * 128 + row]) * sl2;
             }
+            float mn = fmaxf(m_run, mt);
+            bool need = mn > m_run + RESCALE_LOG2;
+            float f = need ? ex2(m_run - mn) : 1.f;    // ex2(-inf) = 0 on the first tile
+            if (need) m_run = mn;
             const float mu = (m_run == NEG_INF) ? 0.f : m_run;
+            // P = exp2(s*sl2 - mu), packed to bf16 as it is produced
             float l0 = 0.f, l1 = 0.f;
+            uint32_t pk0[32], pk1[32];
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fmaf(s[32 * qq + 2 * e], sl2, -mu));
-                    const float p1 = ex2(fmaf(s[32 * qq + 2 * e + 1], sl2, -mu));
-                    l0 += p0;
-                    l1 += p1;
-                    pk[e] = pack_bf16(p0, p1);
-                }
-                tmem_st_x16(tS + 16u * qq, pk);
+            for (int c = 0; c < 128; c += 2) {
+                float x0, x1;
+                ffma2(x0, x1, s[c], s[c + 1], sl2, -mu);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                fadd2(l0, l1, p0, p1);
+                if (c < 64) pk0[c / 2] = pack_bf16(p0, p1);
+                else pk1[(c - 64) / 2] = pack_bf16(p0, p1);
             }
-            tmem_wait_st();
-            l_run += l0 + l1;
-            tc_fence_before();
-            mbar_arrive(BAR(B_PFULL + qi));
-        }
-        if (ok && waitw(BAR(B_OFIN + qi), 0, wc)) {
-            tc_fence_after();
-            const bool valid = qpos < w.cend;
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            __nv_bfloat16 *orow = out + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D;
+            if (!early) {
+                if (!waitw(BAR(B_MX), j & 1, wc)) {
+                    ok = false;
+                    break;
+                }
+                mt = fmaxf(pmj[0 * 128 + row], pmj[1 * 128 + row]) * sl2;
+                mn = fmaxf(m_run, mt);
+                need = mn > m_run + RESCALE_LOG2;
+                if (__any_sync(0xffffffffu, need)) {
+                    // the other half raised the max (rare): rescale this tile's P and sum
+                    f = need ? ex2(m_run - mn) : 1.f;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+                    for (int e = 0; e < 32; ++e) {
+                        pk0[e] = pack_bf16(__uint_as_float(pk0[e] << 16) * f, __uint_as_float(pk0[e] & 0xffff0000u) * f);
+                        pk1[e] = pack_bf16(__uint_as_float(pk1[e] << 16) * f, __uint_as_float(pk1[e] & 0xffff0000u) * f);
+                    }
+                    l0 *= f;
+                    l1 *= f;
+                    if (need) m_run = mn;
+                }
+            }
+            // P(j) may be written, and O rescaled, once PV(j-1) has completed
+            if (j > 0 && !waitw(BAR(B_PFREE), (j - 1) & 1, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + 32u * c, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tmem_st_x32(tO + 32u * c, o);
+                }
+            }
+            l_run = l_run * f + (l0 + l1);
+            tmem_st_x32(tP, pk0);
+            tmem_st_x32(tP + 32u, pk1);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_PFULL));
+        }
+        if (ok && waitw(BAR(B_OFIN), 0, wc)) {
+            tc_fence_after();
+            // total row sum: this half's share plus the other's (exchange phase n;
+            // buffer n&1 was last read before the phase n-1 arrivals)
+            float *pmn = pm + (n & 1) * 256;
+            pmn[half * 128 + row] = l_run;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_MX));
+            ok = waitw(BAR(B_MX), n & 1, wc);
+            const float l_tot = pmn[row] + pmn[128 + row];
+            const bool valid = qpos < w.cend;
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            __nv_bfloat16 *orow = out + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D + (D / 2) * half;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + 32u * c, o);
                 if (valid) {
@@ -380,9 +471,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
-            if (valid)
+            if (ok && valid && half == 0)
                 lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] =
-                    l_run > 0.f ? (m_run + lg2(l_run)) * 0.69314718055994531f : NEG_INF;
+                    l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
         }
         __syncwarp();
         tc_fence_before();
@@ -399,7 +490,7 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
              cudaStream_t st)
 {
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, a.B, a.S, a.Hq, D) || !make_map(&mk, k, a.B, a.S, a.Hkv, D) ||
+    if (!make_map(&mq, q, a.B, a.S, a.Hq, D) || !make_map(&mk, k, a.B, a.S, a.Hkv, D, KT) ||
         !make_map(&mv, v, a.B, a.S, a.Hkv, D))
         return CP_ECUDA;
     static bool attr_done[64] = {};
@@ -412,7 +503,7 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
         attr_done[dev] = true;
     }
     const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
-    a.upc = (g.clen + 2 * QT - 1) / (2 * QT);
+    a.upc = (g.clen + QT - 1) / QT;
     const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
     if (units == 0) return CP_OK;
     if (units > 0x7fffffffLL) return CP_EUNSUPPORTED;

@@ -52,6 +52,35 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// SS / TS MMAs whose descriptors are a base descriptor plus a compile-time
+// offset (16-byte units), added inside the asm so that an unrolled issue
+// sequence keeps only the base descriptors in registers.
+template <uint32_t OFFA, uint32_t OFFB>
+__device__ __forceinline__ void mma_ss_off(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "add.s64 da, %1, %5;\n\tadd.s64 db, %2, %6;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc), "n"(OFFA), "n"(OFFB)
+        : "memory");
+}
+
+template <uint32_t OFFB>
+__device__ __forceinline__ void mma_ts_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "add.s64 db, %2, %5;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "n"(OFFB)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile(
@@ -100,6 +129,34 @@ __device__ __forceinline__ float lg2(float x)
     return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// (d0, d1) = (a0*b + c, a1*b + c) on the paired fp32 pipe
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b, float c)
+{
+    uint64_t A, B, C, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b), "f"(b));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c), "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(R));
+}
+
+// (s0, s1) += (a0, a1) on the paired fp32 pipe
+__device__ __forceinline__ void fadd2(float &s0, float &s1, float a0, float a1)
+{
+    uint64_t S, A, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(S) : "f"(s0), "f"(s1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(R) : "l"(S), "l"(A));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(R));
+}
+
 // two floats -> bf16x2 (round to nearest even), `lo` in the low half
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
@@ -130,14 +187,15 @@ inline EncodeFn get_encode()
     return fn;
 }
 
-// [B][S][H][D] bf16, box = 64 columns x 128 rows of one (b, h), 128B swizzle.
-inline bool make_map(CUtensorMap *m, const void *ptr, int B, int64_t S, int H, int D)
+// [B][S][H][D] bf16, box = 64 columns x box_rows rows of one (b, h), 128B swizzle.
+inline bool make_map(CUtensorMap *m, const void *ptr, int B, int64_t S, int H, int D,
+                     int box_rows = 128)
 {
     EncodeFn enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
-    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

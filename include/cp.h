@@ -74,7 +74,8 @@ int cp_shard_map(int64_t S, int N, int layout, int32_t *pos_host);
 /*
  * cp_schedule_pairs -- walk the exact tile schedule that ring_attn_fwd
  * executes and count, per (rank r, ring step k), the masked-in
- * (query, key) pairs it covers and the 128x128 tile pairs it runs.
+ * (query, key) pairs it covers and the (128-query x 256-key) tile pairs it
+ * runs.
  * "Causal Masking and Load Balancing": under a causal mask contiguous
  * sharding is imbalanced; zigzag equalises the masked-in work per rank.
  *   pairs_host: HOST int64 [N*N], pairs[r*N + k];
@@ -91,8 +92,8 @@ int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_h
  * sketch: source = (rank - step) mod world), masked by global positions of
  * that source ("Causal Masking and Load Balancing"), with the running
  * (out, m, l) folded by online-softmax rescaling ("Algorithmic Mechanics").
- * Fully masked 128x128 tile pairs are skipped, so executed work tracks the
- * masked-in work.
+ * Fully masked (128-query x 256-key) tile pairs are skipped, so executed
+ * work tracks the masked-in work.
  *   q [B][S][Hq][D], k, v [B][S][Hkv][D]: device, dtype CP_F32 or CP_BF16.
  *   out [B][S][Hq][D]: device, same dtype (bf16 rounded to nearest even).
  *   lse [B][Hq][S]: device fp32, lse_i = ln sum_j exp(scale * q_i.k_j).

@@ -63,11 +63,12 @@ def test_schedule_long_sequence_closed_forms(cplib):
         assert pz[r].sum() == 2 * N * c * c + c
     assert pc.sum() == pz.sum() == S * (S + 1) // 2
     assert pc.sum(1)[0] == 33_558_528 and pc.sum(1)[-1] == 1_040_191_488
-    # executed tile pairs: equal per rank under zigzag; only diagonal tiles are partial
+    # executed (128-query x 256-key) tile pairs: equal per rank under zigzag; only
+    # diagonal tiles are partial, so executed work is within 1 % of masked-in work
     per_rank = tz.sum(1)
     assert per_rank.max() - per_rank.min() <= 2
     full_pairs = S * (S + 1) // 2
-    assert tz.sum() * 128 * 128 <= full_pairs * 1.01
+    assert tz.sum() * 128 * 256 <= full_pairs * 1.01
 
 
 def _call_fwd(**kw):
