@@ -21,16 +21,17 @@
 //   warp 0      TMA producer: Q once; K tiles (256 rows) into a 2-deep ring
 //               one tile ahead; V tiles as two 128-row halves; also allocates
 //               and frees the 512 tensor-memory columns.
-//   warp 1      MMA issuer (one thread).
-//   warps 2-3   idle (they complete warpgroup 0 for the register split).
+//   warp 1      issues S = Q K^T (one thread).
+//   warp 2      issues O += P V (one thread).
+//   warp 3      idle (it completes warpgroup 0 for the register split).
 //   warps 4-7   softmax of key columns [0,128), warps 8-11 of [128,256):
 //               one thread per query row.  The halves exchange row maxima
 //               through shared memory (an mbarrier per tile, bounded wait),
 //               so both keep the same running max.
 // Tensor memory columns: S [0,256) fp32, P [256,384) bf16 pairs,
-// O [384,384+D) fp32.  P has its own columns, so the issue order per tile
-//   S(j+1)  (as soon as the softmax has read S(j)),  PV(j)  (once P(j) is written)
-// keeps the tensor pipe busy while the softmax computes exponentials.  The
+// O [384,384+D) fp32.  P has its own columns, so S(j+1) is issued as soon as
+// the softmax has read S(j) and PV(j) once P(j) is written, which keeps the
+// tensor pipe busy while the softmax computes exponentials.  The
 // softmax writes P(j+1) and rescales O only after the commit of PV(j).  O is
 // rescaled only when the running max grows by more than 2^8 (exact: the same
 // stale max is used for P and l).
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(BAR(B_PFULL), 8);
         mbar_init(BAR(B_PFREE), 1);
         mbar_init(BAR(B_OFIN), 1);
-        mbar_init(BAR(B_DRAIN), 1);
+        mbar_init(BAR(B_DRAIN), 2);
         mbar_init(BAR(B_MX), 8);
         *abort_flag = 0;
         fence_mbar_init();
@@ -234,58 +235,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(B_KFULL + (j & 1)), (j >> 1) & 1, dc);
                 for (int x = nv > 2 ? nv - 2 : 0; x < nv; ++x) wait1(BAR(B_VFULL + (x & 1)), (x >> 1) & 1, dc);
             }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
+        } else if ((warp == 1 || warp == 2) && lane == 0) {
+            // ------------------------------------------------------------ MMA issuers
+            // Two issuing threads on different SM sub-partitions: warp 1 issues
+            // S = Q K^T, warp 2 issues O += P V.  They touch disjoint tensor-memory
+            // columns (S vs P and O); every dependency between them goes through
+            // the softmax barriers (S_FREE, P_FULL, P_FREE).  Splitting halves the
+            // issue work each one competes for against two busy softmax warps, and
+            // a wait of one issuer never holds back the other.
             constexpr uint32_t idS = idesc_bf16(128, KT, false);
             constexpr uint32_t idO = idesc_bf16(128, D, true);
             const uint32_t tS = tmem, tP = tmem + 256u, tO = tmem + 384u;
-            // The MMA thread shares its SM sub-partition with two busy softmax
-            // warps, so every instruction it spends between MMAs delays the
-            // tensor pipe: descriptors are built once per buffer and the issue
-            // sequences are unrolled at compile time (offsets are immediates).
-            const uint64_t dQ = sdesc(sQ, 16, 1024);
-            const uint64_t dK0 = sdesc(sK, 16, 1024);
-            const uint64_t dV0 = sdesc(sV, 16384, 1024);
-            auto issue_S = [&](int st) {
-                issue_s_seq<0, D>(tS, dQ, dK0 + (uint64_t)(st * (C::KBYTES >> 4)), idS);
-            };
-            bool ok = n > 0 && wait1(BAR(B_Q), 0, wc) && wait1(BAR(B_KFULL), 0, wc);
-            if (ok) {
-                tc_fence_after();
-                issue_S(0);
-                mma_commit(BAR(B_SFULL));
-                mma_commit(BAR(B_KEMPTY));
-            }
-            for (int j = 0; ok && j < n; ++j) {
-                if (j + 1 < n) {
-                    const int st = (j + 1) & 1;
-                    if (!wait1(BAR(B_SFREE), j & 1, wc) ||
-                        !wait1(BAR(B_KFULL + st), ((j + 1) >> 1) & 1, wc))
-                        break;
+            bool ok = n > 0;
+            if (warp == 1) {
+                const uint64_t dQ = sdesc(sQ, 16, 1024);
+                const uint64_t dK0 = sdesc(sK, 16, 1024);
+                ok = ok && wait1(BAR(B_Q), 0, wc);
+                for (int j = 0; ok && j < n; ++j) {
+                    const int st = j & 1;
+                    if (j > 0 && !wait1(BAR(B_SFREE), (j - 1) & 1, wc)) break;
+                    if (!wait1(BAR(B_KFULL + st), (j >> 1) & 1, wc)) break;
                     tc_fence_after();
-                    issue_S(st);
+                    issue_s_seq<0, D>(tS, dQ, dK0 + (uint64_t)(st * (C::KBYTES >> 4)), idS);
                     mma_commit(BAR(B_SFULL));
                     mma_commit(BAR(B_KEMPTY + st));
                 }
-                if (!wait1(BAR(B_PFULL), j & 1, wc)) break;
-                tc_fence_after();
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (!wait1(BAR(B_VFULL + hh), j & 1, wc)) {
-                        ok = false;
-                        break;
-                    }
+            } else {
+                const uint64_t dV0 = sdesc(sV, 16384, 1024);
+                for (int j = 0; ok && j < n; ++j) {
+                    if (!wait1(BAR(B_PFULL), j & 1, wc)) break;
                     tc_fence_after();
-                    if (hh == 0)
-                        issue_pv_seq<0, 0>(tO, tP, dV0, idO, j > 0 ? 1u : 0u);
-                    else
-                        issue_pv_seq<0, 1>(tO, tP, dV0 + (uint64_t)(C::VBYTES >> 4), idO, 1u);
-                    mma_commit(BAR(B_VEMPTY + hh));
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (!wait1(BAR(B_VFULL + hh), j & 1, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (hh == 0)
+                            issue_pv_seq<0, 0>(tO, tP, dV0, idO, j > 0 ? 1u : 0u);
+                        else
+                            issue_pv_seq<0, 1>(tO, tP, dV0 + (uint64_t)(C::VBYTES >> 4), idO, 1u);
+                        mma_commit(BAR(B_VEMPTY + hh));
+                    }
+                    if (!ok) break;
+                    mma_commit(BAR(B_PFREE));
+                    if (j + 1 == n) mma_commit(BAR(B_OFIN));
                 }
-                if (!ok) break;
-                mma_commit(BAR(B_PFREE));
-                if (j + 1 == n) mma_commit(BAR(B_OFIN));
             }
-            // all MMAs of this block are complete once the drain barrier fires
+            // all MMAs of this thread are complete once the drain barrier (two
+            // arrivals: one commit per issuer) fires
             mma_commit(BAR(B_DRAIN));
             volatile int no_abort = 0;
             WaitCtl dc{a.err, &no_abort, a.limit_ns};
