@@ -73,17 +73,19 @@ __device__ __forceinline__ void ss_seq(uint32_t tD, uint64_t dA, uint64_t dB, ui
     }
 }
 
-// 8 MMAs M=128, N=D, K=16: A (bf16 pairs) from tensor-memory columns
-// [0,32) and [64,96) relative to tA, B MN-major; acc0 = accumulate flag of the first
-template <int KK>
+// 8 MMAs M=128, N=D, K=16: A (bf16 pairs) from tensor memory -- columns
+// [0,32) and [64,96) relative to tA, or [0,64) if CONTIG -- and B MN-major;
+// acc0 = accumulate flag of the first
+template <int KK, bool CONTIG = false>
 __device__ __forceinline__ void ts_seq(uint32_t tD, uint32_t tA, uint64_t dB, uint32_t id,
                                        uint32_t acc0)
 {
     if constexpr (KK < T / 16) {
-        constexpr uint32_t acol = (KK < 4) ? (uint32_t)(KK * 8) : (uint32_t)(64 + (KK - 4) * 8);
+        constexpr uint32_t acol =
+            (CONTIG || KK < 4) ? (uint32_t)(KK * 8) : (uint32_t)(64 + (KK - 4) * 8);
         constexpr uint32_t ob = (uint32_t)((KK * 16 * 128) >> 4);
         mma_ts_off<ob>(tD, tA + acol, dB, id, KK == 0 ? acc0 : 1u);
-        ts_seq<KK + 1>(tD, tA, dB, id, acc0);
+        ts_seq<KK + 1, CONTIG>(tD, tA, dB, id, acc0);
     }
 }
 
@@ -135,10 +137,12 @@ enum {
     Q_VFULL = 5,
     Q_VEMPTY = 7,
     Q_SDP = 9,
-    Q_DS = 10,
+    Q_DS = 10,       // one arrival per gradient warp (8): dS(j) written
     Q_FIN = 11,
-    Q_DRAIN = 12,
-    Q_NBAR = 13
+    Q_DRAIN = 12,    // one commit per issuer (2)
+    Q_SDPFREE = 13,  // one arrival per gradient warp (8): S(j), dP(j) read
+    Q_DSFREE = 14,   // dQ(j) complete: the dS columns may be rewritten
+    Q_NBAR = 15
 };
 
 template <int D>
@@ -192,14 +196,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(BAR(Q_QFULL), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(Q_KFULL + i), 1);
-            mbar_init(BAR(Q_KEMPTY + i), 1);
+            mbar_init(BAR(Q_KEMPTY + i), 2);   // K_j: read by S(j) and by dQ(j)
             mbar_init(BAR(Q_VFULL + i), 1);
             mbar_init(BAR(Q_VEMPTY + i), 1);
         }
         mbar_init(BAR(Q_SDP), 1);
         mbar_init(BAR(Q_DS), 8);
         mbar_init(BAR(Q_FIN), 1);
-        mbar_init(BAR(Q_DRAIN), 1);
+        mbar_init(BAR(Q_DRAIN), 2);
+        mbar_init(BAR(Q_SDPFREE), 8);
+        mbar_init(BAR(Q_DSFREE), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -250,44 +256,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(Q_KFULL + (j & 1)), (j >> 1) & 1, dc);
                 for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) wait1(BAR(Q_VFULL + (j & 1)), (j >> 1) & 1, dc);
             }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
+        } else if ((warp == 1 || warp == 2) && lane == 0) {
+            // ------------------------------------------------------------ MMA issuers
+            // warp 1 issues S = Q K^T and dP = dO V^T as soon as the gradient warps
+            // have read the previous ones; warp 2 issues dQ += dS K.  dS has its
+            // own tensor-memory columns, so the two streams only meet through
+            // the gradient warps' barriers.
             constexpr uint32_t idSP = idesc_bf16(128, T, false);      // S, dP: K-major A and B
             constexpr uint32_t idDQ = idesc_bf16(128, D, true);       // dQ: B = K MN-major
-            const uint32_t tS = tmem, tP = tmem + 128u, tQ = tmem + 256u;
-            const uint64_t dQd = sdesc(sQ, 16, 1024), dDOd = sdesc(sDO, 16, 1024);
-            const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, 16, 1024);
-            const uint64_t dKmn0 = sdesc(sK, 16384, 1024);
-            auto issue_sdp = [&](int st) {
-                const uint64_t so = (uint64_t)(st * (TB >> 4));
-                ss_seq<0, D>(tS, dQd, dK0 + so, idSP);
-                ss_seq<0, D>(tP, dDOd, dV0 + so, idSP);
-            };
-            bool ok = wait1(BAR(Q_QFULL), 0, wc) && wait1(BAR(Q_KFULL), 0, wc) && wait1(BAR(Q_VFULL), 0, wc);
-            if (ok) {
-                tc_fence_after();
-                issue_sdp(0);
-                mma_commit(BAR(Q_SDP));
-                mma_commit(BAR(Q_VEMPTY));
-            }
-            for (int j = 0; ok && j < n; ++j) {
-                const int st = j & 1;
-                if (!wait1(BAR(Q_DS), j & 1, wc)) break;
-                tc_fence_after();
-                // dQ += dS K_j; dS (bf16) sits in columns [0,32) and [64,96) of S
-                ts_seq<0>(tQ, tS, dKmn0 + (uint64_t)(st * (TB >> 4)), idDQ, j > 0 ? 1u : 0u);
-                mma_commit(BAR(Q_KEMPTY + st));
-                if (j + 1 < n) {
-                    const int sn = (j + 1) & 1;
-                    if (!wait1(BAR(Q_KFULL + sn), ((j + 1) >> 1) & 1, wc) ||
-                        !wait1(BAR(Q_VFULL + sn), ((j + 1) >> 1) & 1, wc))
+            const uint32_t tS = tmem, tP = tmem + 128u, tQ = tmem + 256u, tDS = tmem + 384u;
+            bool ok = true;
+            if (warp == 1) {
+                const uint64_t dQd = sdesc(sQ, 16, 1024), dDOd = sdesc(sDO, 16, 1024);
+                const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, 16, 1024);
+                ok = wait1(BAR(Q_QFULL), 0, wc);
+                for (int j = 0; ok && j < n; ++j) {
+                    const int st = j & 1;
+                    if (j > 0 && !wait1(BAR(Q_SDPFREE), (j - 1) & 1, wc)) break;
+                    if (!wait1(BAR(Q_KFULL + st), (j >> 1) & 1, wc) ||
+                        !wait1(BAR(Q_VFULL + st), (j >> 1) & 1, wc))
                         break;
                     tc_fence_after();
-                    issue_sdp(sn);
+                    const uint64_t so = (uint64_t)(st * (TB >> 4));
+                    ss_seq<0, D>(tS, dQd, dK0 + so, idSP);
+                    ss_seq<0, D>(tP, dDOd, dV0 + so, idSP);
                     mma_commit(BAR(Q_SDP));
-                    mma_commit(BAR(Q_VEMPTY + sn));
-                } else {
-                    mma_commit(BAR(Q_FIN));
+                    mma_commit(BAR(Q_VEMPTY + st));
+                    mma_commit(BAR(Q_KEMPTY + st));
+                }
+            } else {
+                const uint64_t dKmn0 = sdesc(sK, 16384, 1024);
+                for (int j = 0; ok && j < n; ++j) {
+                    const int st = j & 1;
+                    if (!wait1(BAR(Q_DS), j & 1, wc) || !wait1(BAR(Q_KFULL + st), (j >> 1) & 1, wc))
+                        break;
+                    tc_fence_after();
+                    // dQ += dS K_j, dS (bf16 pairs) in columns [384, 448)
+                    ts_seq<0, true>(tQ, tDS, dKmn0 + (uint64_t)(st * (TB >> 4)), idDQ, j > 0 ? 1u : 0u);
+                    mma_commit(BAR(Q_KEMPTY + st));
+                    mma_commit(BAR(Q_DSFREE));
+                    if (j + 1 == n) mma_commit(BAR(Q_FIN));
                 }
             }
             mma_commit(BAR(Q_DRAIN));
@@ -313,6 +321,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tS = tmem + lane_off + 64u * half;
         const uint32_t tP = tmem + lane_off + 128u + 64u * half;
         const uint32_t tQ = tmem + lane_off + 256u;
+        const uint32_t tDS = tmem + lane_off + 384u + 32u * half;
         const int qpos = w.q0 + row;
         const bool valid = qpos < w.cend;
         const float sl2 = a.scale * LOG2E;
@@ -333,6 +342,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t sr[64], pr[64];
             tmem_ld_x64(tS, sr);
             tmem_ld_x64(tP, pr);
+            // S(j) and dP(j) may now be overwritten by the next tile's MMAs
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_SDPFREE));
             const int ks = it.start(), kl = it.len();
             int lim = kl;                              // visible columns [0, lim) of the tile
             if (a.causal) {
@@ -350,7 +363,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (2 * e + 1 < lim) d1 = p1 * (__uint_as_float(pr[2 * e + 1]) - dlt);
                 pk[e] = pack_bf16(d0, d1);
             }
-            tmem_st_x32(tS, pk);
+            // dS(j) may be written once dQ(j-1) has read dS(j-1)
+            if (j > 0 && !waitw(BAR(Q_DSFREE), (j - 1) & 1, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_st_x32(tDS, pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
