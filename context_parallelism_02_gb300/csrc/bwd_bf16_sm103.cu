@@ -59,33 +59,47 @@ struct Tile {
 };
 
 // Unrolled issue sequences (compile-time offsets added to base descriptors
-// inside the MMA asm): the MMA thread shares its SM sub-partition with busy
-// gradient warps, so it must spend as few instructions per MMA as possible.
+// inside the MMA asm): the MMA threads share their SM sub-partitions with busy
+// gradient warps, so they spend as few instructions per MMA as possible.
 
-// D/16 MMAs M=128, N=128, K=16, A and B K-major (128-row boxes of 16 KB)
-template <int KK, int D>
+// D/16 MMAs M=128, K=16, A and B K-major; A in 128-row boxes (16 KB), B in
+// boxes of BOXB bytes (16 KB for 128 rows, 8 KB for 64)
+template <int KK, int D, int BOXB>
 __device__ __forceinline__ void ss_seq(uint32_t tD, uint64_t dA, uint64_t dB, uint32_t id)
 {
     if constexpr (KK < D / 16) {
-        constexpr uint32_t o = (uint32_t)(((KK >> 2) * 16384 + (KK & 3) * 32) >> 4);
-        mma_ss_off<o, o>(tD, dA, dB, id, KK > 0 ? 1u : 0u);
-        ss_seq<KK + 1, D>(tD, dA, dB, id);
+        constexpr uint32_t oa = (uint32_t)(((KK >> 2) * 16384 + (KK & 3) * 32) >> 4);
+        constexpr uint32_t ob = (uint32_t)(((KK >> 2) * BOXB + (KK & 3) * 32) >> 4);
+        mma_ss_off<oa, ob>(tD, dA, dB, id, KK > 0 ? 1u : 0u);
+        ss_seq<KK + 1, D, BOXB>(tD, dA, dB, id);
     }
 }
 
-// 8 MMAs M=128, N=D, K=16: A (bf16 pairs) from tensor memory -- columns
-// [0,32) and [64,96) relative to tA, or [0,64) if CONTIG -- and B MN-major;
-// acc0 = accumulate flag of the first
-template <int KK, bool CONTIG = false>
-__device__ __forceinline__ void ts_seq(uint32_t tD, uint32_t tA, uint64_t dB, uint32_t id,
-                                       uint32_t acc0)
+// D/16 MMAs M=128, K=16, A (bf16 pairs) from tensor memory columns tA + 8 KK,
+// B K-major in 128-row boxes
+template <int KK, int D>
+__device__ __forceinline__ void tsk_seq(uint32_t tD, uint32_t tA, uint64_t dB, uint32_t id)
 {
-    if constexpr (KK < T / 16) {
-        constexpr uint32_t acol =
-            (CONTIG || KK < 4) ? (uint32_t)(KK * 8) : (uint32_t)(64 + (KK - 4) * 8);
-        constexpr uint32_t ob = (uint32_t)((KK * 16 * 128) >> 4);
+    if constexpr (KK < D / 16) {
+        constexpr uint32_t ob = (uint32_t)(((KK >> 2) * 16384 + (KK & 3) * 32) >> 4);
+        mma_ts_off<ob>(tD, tA + KK * 8, dB, id, KK > 0 ? 1u : 0u);
+        tsk_seq<KK + 1, D>(tD, tA, dB, id);
+    }
+}
+
+// NK MMAs M=128, N=D, K=16: A (bf16 pairs) from tensor memory, B MN-major
+// (k-steps of 16 rows, 2048 B); A columns relative to tA: 8 KK (MAP 0), or
+// 32 (KK/2) + 8 (KK%2) (MAP 1: two runs of 16 columns, 32 apart).
+// acc0 = accumulate flag of the first MMA.
+template <int KK, int NK, int MAP>
+__device__ __forceinline__ void ts_mn_seq(uint32_t tD, uint32_t tA, uint64_t dB, uint32_t id,
+                                          uint32_t acc0)
+{
+    if constexpr (KK < NK) {
+        constexpr uint32_t acol = MAP == 0 ? (uint32_t)(KK * 8) : (uint32_t)(32 * (KK >> 1) + 8 * (KK & 1));
+        constexpr uint32_t ob = (uint32_t)((KK * 2048) >> 4);
         mma_ts_off<ob>(tD, tA + acol, dB, id, KK == 0 ? acc0 : 1u);
-        ts_seq<KK + 1, CONTIG>(tD, tA, dB, id, acc0);
+        ts_mn_seq<KK + 1, NK, MAP>(tD, tA, dB, id, acc0);
     }
 }
 
@@ -129,33 +143,64 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__r
 }
 
 // ----------------------------------------------------------------------------- dQ
+//
+// Query-stationary.  Tensor memory (columns): S [0,128), dP [128,256), the dQ
+// accumulator [256, 256+D), dS in bf16 pairs [256+D, 320+D), and Q in bf16
+// pairs [320+D, 320+3D/2).  Q is the same for every KV tile of the block, so
+// the gradient warps write it into tensor memory once and S = Q K^T takes its
+// A operand from there; shared memory holds dO, four K stages and two V stages.
+//
+// S(j) and dP(j) have their own barriers both ways, so S(j+1) is issued as
+// soon as the gradient warps have read S(j) and runs while they read dP(j)
+// and compute; dQ(j) comes last.  K_j is read by S(j) and by dQ(j); with the
+// MMA order S(j+1), dP(j+1), dQ(j) the load of K(j+4) into the stage of K(j)
+// has three tile groups of MMAs to land.
 
+constexpr int Q_KST = 4;
 enum {
-    Q_QFULL = 0,
-    Q_KFULL = 1,
-    Q_KEMPTY = 3,
-    Q_VFULL = 5,
-    Q_VEMPTY = 7,
-    Q_SDP = 9,
-    Q_DS = 10,       // one arrival per gradient warp (8): dS(j) written
-    Q_FIN = 11,
-    Q_DRAIN = 12,    // one commit per issuer (2)
-    Q_SDPFREE = 13,  // one arrival per gradient warp (8): S(j), dP(j) read
-    Q_DSFREE = 14,   // dQ(j) complete: the dS columns may be rewritten
-    Q_NBAR = 15
+    Q_QTM = 0,       // Q written into tensor memory: one arrival per gradient warp (8)
+    Q_DOFULL = 1,    // dO tile landed
+    Q_KFULL = 2,     // Q_KST stages
+    Q_KEMPTY = 6,    // Q_KST stages; commits after S(j) and after dQ(j)
+    Q_VFULL = 10,    // 2 stages
+    Q_VEMPTY = 12,   // 2 stages
+    Q_SDONE = 14,    // S(j) complete
+    Q_PDONE = 15,    // dP(j) complete
+    Q_SFREE = 16,    // S(j) read by the gradient warps (8 arrivals)
+    Q_PFREE = 17,    // dP(j) read (8 arrivals)
+    Q_DS = 18,       // dS(j) written (8 arrivals)
+    Q_DSFREE = 19,   // dQ(j) complete: the dS columns may be rewritten
+    Q_FIN = 20,
+    Q_DRAIN = 21,    // one commit per issuer (2)
+    Q_NBAR = 22
 };
 
 template <int D>
 struct DqCfg {
     static constexpr int TB = Tile<D>::BYTES;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_DO = TB;
-    static constexpr int OFF_K = 2 * TB;     // 2 stages
-    static constexpr int OFF_V = 4 * TB;     // 2 stages
-    static constexpr int OFF_BAR = 6 * TB;
+    static constexpr int OFF_DO = 0;
+    static constexpr int OFF_K = TB;                    // Q_KST stages
+    static constexpr int OFF_V = (1 + Q_KST) * TB;      // 2 stages
+    static constexpr int OFF_BAR = (3 + Q_KST) * TB;
     static constexpr int OFF_MISC = OFF_BAR + 8 * Q_NBAR;
-    static constexpr int NEED = OFF_MISC + 16 + 1024;
+    static constexpr int NEED = OFF_MISC + 16;
     static constexpr int SMEM = NEED > 120 * 1024 ? NEED : 120 * 1024;
+    static_assert(SMEM <= 232448, "dQ kernel shared memory");
+    static constexpr uint32_t TM_S = 0, TM_P = 128, TM_DQ = 256, TM_DS = 256 + D, TM_Q = 320 + D;
+    static_assert(TM_Q + D / 2 <= 512, "dQ kernel tensor memory");
+};
+
+// stage index and phase parity of a ring of NS buffers, advanced once per use
+template <int NS>
+struct Ring {
+    int st = 0, ph = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++st == NS) {
+            st = 0;
+            ph ^= 1;
+        }
+    }
 };
 
 struct BwdArgs {
@@ -169,43 +214,50 @@ struct BwdArgs {
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                  const BwdArgs a, const float *__restrict__ lse, const float *__restrict__ delta,
-                  __nv_bfloat16 *__restrict__ dq)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmDO, const BwdArgs a,
+                  const __nv_bfloat16 *__restrict__ q, const float *__restrict__ lse,
+                  const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dq)
 {
     using C = DqCfg<D>;
     constexpr int TB = C::TB;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + C::OFF_Q, sDO = base + C::OFF_DO, sK = base + C::OFF_K,
-                   sV = base + C::OFF_V, bar0 = base + C::OFF_BAR;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_u32(smem_raw);
+    if (base & 1023u) {   // the 128B-swizzled tiles need 1 KB alignment
+        if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_TIMEOUT);
+        return;
+    }
+    const uint32_t sDO = base + C::OFF_DO, sK = base + C::OFF_K, sV = base + C::OFF_V,
+                   bar0 = base + C::OFF_BAR;
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::OFF_MISC + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + C::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
-    const Unit w = decode_unit(g, a.B, a.Hq, 0, a.N, a.upc, T, blockIdx.x);
+    const Unit w = decode_unit_grouped(g, a.B, a.Hq, a.upc, T, blockIdx.x);
     const int kvh = w.h / (a.Hq / a.Hkv);
     const int n = KvIter<T>::count(g, w.r, w.qmax);
 
     if (threadIdx.x == 0) {
-        mbar_init(BAR(Q_QFULL), 1);
-        for (int i = 0; i < 2; ++i) {
+        mbar_init(BAR(Q_QTM), 8);
+        mbar_init(BAR(Q_DOFULL), 1);
+        for (int i = 0; i < Q_KST; ++i) {
             mbar_init(BAR(Q_KFULL + i), 1);
-            mbar_init(BAR(Q_KEMPTY + i), 2);   // K_j: read by S(j) and by dQ(j)
+            mbar_init(BAR(Q_KEMPTY + i), 2);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(Q_VFULL + i), 1);
             mbar_init(BAR(Q_VEMPTY + i), 1);
         }
-        mbar_init(BAR(Q_SDP), 1);
+        mbar_init(BAR(Q_SDONE), 1);
+        mbar_init(BAR(Q_PDONE), 1);
+        mbar_init(BAR(Q_SFREE), 8);
+        mbar_init(BAR(Q_PFREE), 8);
         mbar_init(BAR(Q_DS), 8);
+        mbar_init(BAR(Q_DSFREE), 1);
         mbar_init(BAR(Q_FIN), 1);
         mbar_init(BAR(Q_DRAIN), 2);
-        mbar_init(BAR(Q_SDPFREE), 8);
-        mbar_init(BAR(Q_DSFREE), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -224,76 +276,92 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
         if (warp == 0 && lane == 0) {
-            // ------------------------------------------------------------ producer
-            const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
-            mbar_arrive_expect_tx(BAR(Q_QFULL), 2 * TB);
-            for (int bx = 0; bx < D / 64; ++bx) {
-                tma_load4(sQ + bx * 16384, &tmQ, BAR(Q_QFULL), bx * 64, w.h, w.q0, w.b, pol_q);
-                tma_load4(sDO + bx * 16384, &tmDO, BAR(Q_QFULL), bx * 64, w.h, w.q0, w.b, pol_q);
-            }
+            // ------------------------------------------------------------ K producer
+            const uint64_t pol_kv = policy_evict_last();
             KvIter<T> it;
             it.begin(g, w.r, w.qmax);
-            int nk = 0, nv = 0;
-            for (int j = 0; j < n; ++j, it.next()) {
-                const int st = j & 1, row = it.start();
-                if (j >= 2 && !wait1(BAR(Q_KEMPTY + st), ((j >> 1) - 1) & 1, wc)) break;
-                mbar_arrive_expect_tx(BAR(Q_KFULL + st), TB);
+            int nk = 0;
+            Ring<Q_KST> kr;
+            for (int j = 0; j < n; ++j, it.next(), kr.next()) {
+                if (j >= Q_KST && !wait1(BAR(Q_KEMPTY + kr.st), kr.ph ^ 1, wc)) break;
+                mbar_arrive_expect_tx(BAR(Q_KFULL + kr.st), TB);
                 for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load4(sK + st * TB + bx * 16384, &tmK, BAR(Q_KFULL + st), bx * 64, kvh, row,
-                              w.b, pol_kv);
+                    tma_load4(sK + kr.st * TB + bx * 16384, &tmK, BAR(Q_KFULL + kr.st), bx * 64, kvh,
+                              it.start(), w.b, pol_kv);
                 ++nk;
-                if (j >= 2 && !wait1(BAR(Q_VEMPTY + st), ((j >> 1) - 1) & 1, wc)) break;
-                mbar_arrive_expect_tx(BAR(Q_VFULL + st), TB);
+            }
+            if (*abort_flag) {
+                // wait (bounded) for the copies still in flight before the block exits
+                volatile int no_abort = 0;
+                WaitCtl dc{a.err, &no_abort, a.limit_ns};
+                for (int j = nk > Q_KST ? nk - Q_KST : 0; j < nk; ++j)
+                    wait1(BAR(Q_KFULL + j % Q_KST), (j / Q_KST) & 1, dc);
+            }
+        } else if (warp == 3 && lane == 0) {
+            // ------------------------------------------------------------ dO and V producer
+            const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+            mbar_arrive_expect_tx(BAR(Q_DOFULL), TB);
+            for (int bx = 0; bx < D / 64; ++bx)
+                tma_load4(sDO + bx * 16384, &tmDO, BAR(Q_DOFULL), bx * 64, w.h, w.q0, w.b, pol_q);
+            KvIter<T> it;
+            it.begin(g, w.r, w.qmax);
+            int nv = 0;
+            for (int j = 0; j < n; ++j, it.next()) {
+                const int sv = j & 1;
+                if (j >= 2 && !wait1(BAR(Q_VEMPTY + sv), ((j >> 1) - 1) & 1, wc)) break;
+                mbar_arrive_expect_tx(BAR(Q_VFULL + sv), TB);
                 for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load4(sV + st * TB + bx * 16384, &tmV, BAR(Q_VFULL + st), bx * 64, kvh, row,
-                              w.b, pol_kv);
+                    tma_load4(sV + sv * TB + bx * 16384, &tmV, BAR(Q_VFULL + sv), bx * 64, kvh,
+                              it.start(), w.b, pol_kv);
                 ++nv;
             }
             if (*abort_flag) {
                 volatile int no_abort = 0;
                 WaitCtl dc{a.err, &no_abort, a.limit_ns};
-                wait1(BAR(Q_QFULL), 0, dc);
-                for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(Q_KFULL + (j & 1)), (j >> 1) & 1, dc);
+                wait1(BAR(Q_DOFULL), 0, dc);
                 for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) wait1(BAR(Q_VFULL + (j & 1)), (j >> 1) & 1, dc);
             }
         } else if ((warp == 1 || warp == 2) && lane == 0) {
             // ------------------------------------------------------------ MMA issuers
-            // warp 1 issues S = Q K^T and dP = dO V^T as soon as the gradient warps
-            // have read the previous ones; warp 2 issues dQ += dS K.  dS has its
-            // own tensor-memory columns, so the two streams only meet through
-            // the gradient warps' barriers.
-            constexpr uint32_t idSP = idesc_bf16(128, T, false);      // S, dP: K-major A and B
-            constexpr uint32_t idDQ = idesc_bf16(128, D, true);       // dQ: B = K MN-major
-            const uint32_t tS = tmem, tP = tmem + 128u, tQ = tmem + 256u, tDS = tmem + 384u;
+            // warp 1: S = Q K^T (A = Q from tensor memory) and dP = dO V^T;
+            // warp 2: dQ += dS K.
+            constexpr uint32_t idSP = idesc_bf16(128, T, false);     // K-major A and B
+            constexpr uint32_t idDQ = idesc_bf16(128, D, true);      // B = K MN-major
+            const uint32_t tS = tmem + C::TM_S, tP = tmem + C::TM_P, tDQ = tmem + C::TM_DQ,
+                           tDS = tmem + C::TM_DS, tQ = tmem + C::TM_Q;
             bool ok = true;
             if (warp == 1) {
-                const uint64_t dQd = sdesc(sQ, 16, 1024), dDOd = sdesc(sDO, 16, 1024);
+                const uint64_t dDOd = sdesc(sDO, 16, 1024);
                 const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, 16, 1024);
-                ok = wait1(BAR(Q_QFULL), 0, wc);
-                for (int j = 0; ok && j < n; ++j) {
-                    const int st = j & 1;
-                    if (j > 0 && !wait1(BAR(Q_SDPFREE), (j - 1) & 1, wc)) break;
-                    if (!wait1(BAR(Q_KFULL + st), (j >> 1) & 1, wc) ||
-                        !wait1(BAR(Q_VFULL + st), (j >> 1) & 1, wc))
+                ok = wait1(BAR(Q_QTM), 0, wc) && wait1(BAR(Q_DOFULL), 0, wc);
+                Ring<Q_KST> kr;
+                for (int j = 0; ok && j < n; ++j, kr.next()) {
+                    const int sv = j & 1;
+                    if ((j > 0 && !wait1(BAR(Q_SFREE), (j - 1) & 1, wc)) ||
+                        !wait1(BAR(Q_KFULL + kr.st), kr.ph, wc))
                         break;
                     tc_fence_after();
-                    const uint64_t so = (uint64_t)(st * (TB >> 4));
-                    ss_seq<0, D>(tS, dQd, dK0 + so, idSP);
-                    ss_seq<0, D>(tP, dDOd, dV0 + so, idSP);
-                    mma_commit(BAR(Q_SDP));
-                    mma_commit(BAR(Q_VEMPTY + st));
-                    mma_commit(BAR(Q_KEMPTY + st));
+                    tsk_seq<0, D>(tS, tQ, dK0 + (uint64_t)(kr.st * (TB >> 4)), idSP);
+                    mma_commit(BAR(Q_SDONE));
+                    mma_commit(BAR(Q_KEMPTY + kr.st));
+                    if ((j > 0 && !wait1(BAR(Q_PFREE), (j - 1) & 1, wc)) ||
+                        !wait1(BAR(Q_VFULL + sv), (j >> 1) & 1, wc))
+                        break;
+                    tc_fence_after();
+                    ss_seq<0, D, 16384>(tP, dDOd, dV0 + (uint64_t)(sv * (TB >> 4)), idSP);
+                    mma_commit(BAR(Q_PDONE));
+                    mma_commit(BAR(Q_VEMPTY + sv));
                 }
             } else {
                 const uint64_t dKmn0 = sdesc(sK, 16384, 1024);
-                for (int j = 0; ok && j < n; ++j) {
-                    const int st = j & 1;
-                    if (!wait1(BAR(Q_DS), j & 1, wc) || !wait1(BAR(Q_KFULL + st), (j >> 1) & 1, wc))
+                Ring<Q_KST> kr;
+                for (int j = 0; ok && j < n; ++j, kr.next()) {
+                    if (!wait1(BAR(Q_DS), j & 1, wc) || !wait1(BAR(Q_KFULL + kr.st), kr.ph, wc))
                         break;
                     tc_fence_after();
-                    // dQ += dS K_j, dS (bf16 pairs) in columns [384, 448)
-                    ts_seq<0, true>(tQ, tDS, dKmn0 + (uint64_t)(st * (TB >> 4)), idDQ, j > 0 ? 1u : 0u);
-                    mma_commit(BAR(Q_KEMPTY + st));
+                    ts_mn_seq<0, T / 16, 0>(tDQ, tDS, dKmn0 + (uint64_t)(kr.st * (TB >> 4)), idDQ,
+                                            j > 0 ? 1u : 0u);
+                    mma_commit(BAR(Q_KEMPTY + kr.st));
                     mma_commit(BAR(Q_DSFREE));
                     if (j + 1 == n) mma_commit(BAR(Q_FIN));
                 }
@@ -318,12 +386,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + 64u * half;
-        const uint32_t tP = tmem + lane_off + 128u + 64u * half;
-        const uint32_t tQ = tmem + lane_off + 256u;
-        const uint32_t tDS = tmem + lane_off + 384u + 32u * half;
+        const uint32_t tS = tmem + lane_off + C::TM_S + 64u * half;
+        const uint32_t tP = tmem + lane_off + C::TM_P + 64u * half;
+        const uint32_t tDQ = tmem + lane_off + C::TM_DQ;
+        const uint32_t tDS = tmem + lane_off + C::TM_DS + 32u * half;
         const int qpos = w.q0 + row;
         const bool valid = qpos < w.cend;
+        {
+            // this half's D/2 elements of the Q row, as D/4 bf16 pairs (rows past the
+            // unit's chunk are zero; their results are never stored)
+            uint32_t qv[D / 4];
+            if (valid) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    q + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D + (D / 2) * half);
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    const uint4 x = src[i];
+                    qv[4 * i] = x.x;
+                    qv[4 * i + 1] = x.y;
+                    qv[4 * i + 2] = x.z;
+                    qv[4 * i + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < D / 4; ++i) qv[i] = 0u;
+            }
+            const uint32_t tQ = tmem + lane_off + C::TM_Q + (D / 4) * half;
+            if constexpr (D == 128) tmem_st_x32(tQ, qv);
+            else tmem_st_x16(tQ, qv);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_QTM));
+        }
         const float sl2 = a.scale * LOG2E;
         float lse2 = 0.f, dlt = 0.f;
         if (valid) {
@@ -334,18 +429,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         KvIter<T> it;
         it.begin(g, w.r, w.qmax);
         for (int j = 0; j < n; ++j, it.next()) {
-            if (!waitw(BAR(Q_SDP), j & 1, wc)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sr[64], pr[64];
-            tmem_ld_x64(tS, sr);
-            tmem_ld_x64(tP, pr);
-            // S(j) and dP(j) may now be overwritten by the next tile's MMAs
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(Q_SDPFREE));
             const int ks = it.start(), kl = it.len();
             int lim = kl;                              // visible columns [0, lim) of the tile
             if (a.causal) {
@@ -353,16 +436,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 lim = c < lim ? c : lim;
             }
             lim -= 64 * half;                          // in this half's local columns
+            if (!waitw(BAR(Q_SDONE), j & 1, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[64];
+            tmem_ld_x64(tS, sr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_SFREE));   // S(j+1) may be issued
+            float p[64];
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                p[e] = e < lim ? ex2(fmaf(__uint_as_float(sr[e]), sl2, -lse2)) : 0.f;
+            if (!waitw(BAR(Q_PDONE), j & 1, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t pr[64];
+            tmem_ld_x64(tP, pr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_PFREE));   // dP(j+1) may be issued
             uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                float d0 = 0.f, d1 = 0.f;
-                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), sl2, -lse2));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -lse2));
-                if (2 * e < lim) d0 = p0 * (__uint_as_float(pr[2 * e]) - dlt);
-                if (2 * e + 1 < lim) d1 = p1 * (__uint_as_float(pr[2 * e + 1]) - dlt);
-                pk[e] = pack_bf16(d0, d1);
-            }
+            for (int e = 0; e < 32; ++e)
+                pk[e] = pack_bf16(p[2 * e] * (__uint_as_float(pr[2 * e]) - dlt),
+                                  p[2 * e + 1] * (__uint_as_float(pr[2 * e + 1]) - dlt));
             // dS(j) may be written once dQ(j-1) has read dS(j-1)
             if (j > 0 && !waitw(BAR(Q_DSFREE), (j - 1) & 1, wc)) {
                 ok = false;
@@ -383,7 +485,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld_x32(tQ + HD * half + 32u * c, o);
+                tmem_ld_x32(tDQ + HD * half + 32u * c, o);
                 if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
@@ -407,66 +509,90 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ----------------------------------------------------------------------------- dK, dV
+//
+// Key-stationary, in half tiles of 64 queries: for each query tile the block
+// visits (QIter order), two half steps s.  Per half step: S^T = K Q_s^T and
+// dP^T = V dO_s^T (M=128 keys, N=64) into tensor-memory buffer s%2; gradient
+// warpgroup s%2 turns them into P^T and dS^T (bf16 pairs, written over the
+// first half of the columns it read); then dV += P^T dO_s and dK += dS^T Q_s
+// (N=D, K=64).  With two buffers and one warpgroup per buffer, the MMAs of
+// step s+1 run while warpgroup s%2 works on step s, and the MMA issue order
+// dV/dK(s), S^T/dP^T(s+2) reuses buffer s%2 only after it has been read.
+// Each gradient thread handles all 64 columns of its steps, so it moves them
+// with two 64-column tensor-memory loads and two 32-column stores.
+//
+// Tensor memory (columns): buffer x at 128x: S^T [0,64), dP^T [64,128);
+// dV [256, 256+D), dK [256+D, 256+2D).  Shared memory: K and V (128 rows),
+// K_QST half stages of (Q_s, dO_s) 64-row tiles, and their lse / Delta.
 
+constexpr int K_QST = 4;
 enum {
     K_KVFULL = 0,
-    K_QFULL = 1,    // 2 stages
-    K_QEMPTY = 3,   // 2 stages
-    K_SDP = 5,
-    K_PDS = 6,
-    K_FIN = 7,
-    K_DRAIN = 8,
-    K_NBAR = 9
+    K_QFULL = 1,                  // K_QST half stages
+    K_QEMPTY = 1 + K_QST,         // K_QST half stages
+    K_SDP = 1 + 2 * K_QST,        // 2 buffers: S^T, dP^T complete
+    K_PDS = 3 + 2 * K_QST,        // 2 buffers: P^T, dS^T written (4 arrivals: one warpgroup)
+    K_FIN = 5 + 2 * K_QST,
+    K_DRAIN = 6 + 2 * K_QST,
+    K_NBAR = 7 + 2 * K_QST
 };
 
 template <int D>
 struct DkvCfg {
-    static constexpr int TB = Tile<D>::BYTES;
+    static constexpr int TB = Tile<D>::BYTES;            // 128 rows
+    static constexpr int HB = TB / 2;                    // 64 rows
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = TB;
-    static constexpr int OFF_Q = 2 * TB;      // 2 stages
-    static constexpr int OFF_DO = 4 * TB;     // 2 stages
-    static constexpr int OFF_STAT = 6 * TB;   // 2 stages x (lse2[128], delta[128]) fp32
-    static constexpr int OFF_BAR = OFF_STAT + 2 * 2 * 128 * 4;
+    static constexpr int OFF_Q = 2 * TB;                 // K_QST stages of (Q_s, dO_s)
+    static constexpr int STAGE = 2 * HB;
+    static constexpr int OFF_STAT = OFF_Q + K_QST * STAGE;   // K_QST x (lse2[64], delta[64]) fp32
+    static constexpr int OFF_BAR = OFF_STAT + K_QST * 2 * 64 * 4;
     static constexpr int OFF_MISC = OFF_BAR + 8 * K_NBAR;
-    static constexpr int NEED = OFF_MISC + 16 + 1024;
+    static constexpr int NEED = OFF_MISC + 16;
     static constexpr int SMEM = NEED > 120 * 1024 ? NEED : 120 * 1024;
+    static_assert(SMEM <= 232448, "dK/dV kernel shared memory");
+    static constexpr uint32_t TM_DV = 256, TM_DK = 256 + D;
+    static_assert(TM_DK + D <= 512, "dK/dV kernel tensor memory");
 };
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDOh,
                     const BwdArgs a, const float *__restrict__ lse, const float *__restrict__ delta,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv)
 {
     using C = DkvCfg<D>;
-    constexpr int TB = C::TB;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
+    constexpr int TB = C::TB, HB = C::HB;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_u32(smem_raw);
+    if (base & 1023u) {   // the 128B-swizzled tiles need 1 KB alignment
+        if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_TIMEOUT);
+        return;
+    }
     const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQ = base + C::OFF_Q,
-                   sDO = base + C::OFF_DO, bar0 = base + C::OFF_BAR;
-    float *stat = reinterpret_cast<float *>(gbase + C::OFF_STAT);   // [stage][lse2 | delta][128]
+                   bar0 = base + C::OFF_BAR;
+    float *stat = reinterpret_cast<float *>(smem_raw + C::OFF_STAT);   // [stage][lse2 | delta][64]
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::OFF_MISC + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + C::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
     const KvUnit w = decode_kv_unit<T>(g, a.B, a.Hkv, a.tpc, blockIdx.x);
     const int grp = a.Hq / a.Hkv;
-    const int n = QIter<T>::count(g, w.src, w.ks, grp);
+    const int ns = 2 * QIter<T>::count(g, w.src, w.ks, grp);   // half steps
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(K_KVFULL), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < K_QST; ++i) {
             mbar_init(BAR(K_QFULL + i), 1);
             mbar_init(BAR(K_QEMPTY + i), 1);
         }
-        mbar_init(BAR(K_SDP), 1);
-        mbar_init(BAR(K_PDS), 8);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(BAR(K_SDP + i), 1);
+            mbar_init(BAR(K_PDS + i), 4);
+        }
         mbar_init(BAR(K_FIN), 1);
         mbar_init(BAR(K_DRAIN), 1);
         *abort_flag = 0;
@@ -499,13 +625,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             QIter<T> it;
             it.begin(g, w.src, w.ks, w.g * grp, grp);
             int issued = 0;
-            for (int i = 0; i < n; ++i, it.next()) {
-                const int st = i & 1;
-                if (i >= 2 && !waitw(BAR(K_QEMPTY + st), ((i >> 1) - 1) & 1, wc)) break;
-                const int qa = it.start(), ql = it.len(), h = it.head();
-                // per-row statistics of the query tile: lse (log2 units) and Delta
-                float *ls = stat + st * 256, *dl = ls + 128;
-                for (int e = lane; e < 128; e += 32) {
+            Ring<K_QST> qr;
+            for (int s = 0; s < ns; ++s, qr.next()) {
+                if (s >= K_QST && !waitw(BAR(K_QEMPTY + qr.st), qr.ph ^ 1, wc)) break;
+                const int hs = s & 1;
+                const int qa = it.start() + 64 * hs, ql = it.len() - 64 * hs, h = it.head();
+                // per-row statistics of the half tile: lse (log2 units) and Delta
+                float *ls = stat + qr.st * 128, *dl = ls + 64;
+                for (int e = lane; e < 64; e += 32) {
                     float l2 = 0.f, dd = 0.f;
                     if (e < ql) {
                         const int64_t off = ((int64_t)w.b * a.Hq + h) * a.S + qa + e;
@@ -517,46 +644,67 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(BAR(K_QFULL + st), 2 * TB);
+                    const uint32_t sq = sQ + qr.st * C::STAGE;
+                    mbar_arrive_expect_tx(BAR(K_QFULL + qr.st), 2 * HB);
                     for (int bx = 0; bx < D / 64; ++bx) {
-                        tma_load4(sQ + st * TB + bx * 16384, &tmQ, BAR(K_QFULL + st), bx * 64, h, qa,
-                                  w.b, pol_q);
-                        tma_load4(sDO + st * TB + bx * 16384, &tmDO, BAR(K_QFULL + st), bx * 64, h,
-                                  qa, w.b, pol_q);
+                        tma_load4(sq + bx * 8192, &tmQh, BAR(K_QFULL + qr.st), bx * 64, h, qa, w.b, pol_q);
+                        tma_load4(sq + HB + bx * 8192, &tmDOh, BAR(K_QFULL + qr.st), bx * 64, h, qa, w.b,
+                                  pol_q);
                     }
                 }
                 __syncwarp();
-                issued = i + 1;
+                issued = s + 1;
+                if (hs) it.next();
             }
             if (lane == 0 && *abort_flag) {
+                // wait (bounded) for the copies still in flight before the block exits
                 volatile int no_abort = 0;
                 WaitCtl dc{a.err, &no_abort, a.limit_ns};
                 wait1(BAR(K_KVFULL), 0, dc);
-                for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-                    wait1(BAR(K_QFULL + (i & 1)), (i >> 1) & 1, dc);
+                for (int s = issued > K_QST ? issued - K_QST : 0; s < issued; ++s)
+                    wait1(BAR(K_QFULL + s % K_QST), (s / K_QST) & 1, dc);
             }
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------------------ MMA issuer
-            constexpr uint32_t idSP = idesc_bf16(128, T, false);    // S^T, dP^T
+            constexpr uint32_t idSP = idesc_bf16(128, 64, false);   // S^T, dP^T: N = 64 queries
             constexpr uint32_t idKV = idesc_bf16(128, D, true);     // dV, dK: B MN-major
-            const uint32_t tS = tmem, tP = tmem + 128u, tV = tmem + 256u, tK = tmem + 384u;
             const uint64_t dKd = sdesc(sK, 16, 1024), dVd = sdesc(sV, 16, 1024);
-            const uint64_t dQ0 = sdesc(sQ, 16, 1024), dDO0 = sdesc(sDO, 16, 1024);
-            const uint64_t dQmn0 = sdesc(sQ, 16384, 1024), dDOmn0 = sdesc(sDO, 16384, 1024);
+            const uint64_t dQ0 = sdesc(sQ, 16, 1024);                 // Q_s K-major (64-row boxes)
+            const uint64_t dQmn0 = sdesc(sQ, 8192, 1024);            // Q_s, dO_s MN-major
+            const uint32_t tDV = tmem + C::TM_DV, tDK = tmem + C::TM_DK;
+            // S^T(s), dP^T(s) into buffer s%2 from half stage `st`
+            auto issue_sdp = [&](int s, int st) {
+                const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
+                const uint64_t so = (uint64_t)(st * (C::STAGE >> 4));
+                ss_seq<0, D, 8192>(tb, dKd, dQ0 + so, idSP);
+                ss_seq<0, D, 8192>(tb + 64u, dVd, dQ0 + so + (uint64_t)(HB >> 4), idSP);
+                mma_commit(BAR(K_SDP + (s & 1)));
+            };
             bool ok = wait1(BAR(K_KVFULL), 0, wc);
-            for (int i = 0; ok && i < n; ++i) {
-                const int st = i & 1;
-                if (!wait1(BAR(K_QFULL + st), (i >> 1) & 1, wc)) break;
+            Ring<K_QST> rs;      // stage of half step s
+            Ring<K_QST> rn;      // stage of half step s + 2
+            for (int i = 0; ok && i < 2 && i < ns; ++i, rn.next()) {
+                if (!wait1(BAR(K_QFULL + rn.st), rn.ph, wc)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint64_t so = (uint64_t)(st * (TB >> 4));
-                ss_seq<0, D>(tS, dKd, dQ0 + so, idSP);
-                ss_seq<0, D>(tP, dVd, dDO0 + so, idSP);
-                mma_commit(BAR(K_SDP));
-                if (!wait1(BAR(K_PDS), i & 1, wc)) break;
+                issue_sdp(i, rn.st);
+            }
+            for (int s = 0; ok && s < ns; ++s, rs.next(), rn.next()) {
+                if (!wait1(BAR(K_PDS + (s & 1)), (s >> 1) & 1, wc)) break;
                 tc_fence_after();
-                ts_seq<0>(tV, tS, dDOmn0 + (uint64_t)(st * (TB >> 4)), idKV, i > 0 ? 1u : 0u);
-                ts_seq<0>(tK, tP, dQmn0 + (uint64_t)(st * (TB >> 4)), idKV, i > 0 ? 1u : 0u);
-                mma_commit(BAR(K_QEMPTY + st));
+                const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
+                const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
+                // dV += P^T dO_s, dK += dS^T Q_s (K = 64 queries: 4 MMAs each)
+                ts_mn_seq<0, 4, 0>(tDV, tb, dQmn0 + so + (uint64_t)(HB >> 4), idKV, s > 0 ? 1u : 0u);
+                ts_mn_seq<0, 4, 0>(tDK, tb + 64u, dQmn0 + so, idKV, s > 0 ? 1u : 0u);
+                mma_commit(BAR(K_QEMPTY + rs.st));
+                if (s + 2 < ns) {
+                    if (!wait1(BAR(K_QFULL + rn.st), rn.ph, wc)) break;
+                    tc_fence_after();
+                    issue_sdp(s + 2, rn.st);
+                }
             }
             mma_commit(BAR(K_FIN));
             mma_commit(BAR(K_DRAIN));
@@ -575,59 +723,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_GRAD));
         // ------------------------------------------------------------ P^T, dS^T
-        const int half = (warp - 4) >> 2;           // query columns [64*half, 64*half+64)
+        const int half = (warp - 4) >> 2;           // warpgroup: half steps s with s % 2 == half
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;        // key row of the tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + 64u * half;
-        const uint32_t tP = tmem + lane_off + 128u + 64u * half;
+        const uint32_t tb = tmem + lane_off + 128u * (uint32_t)half;
         const int kpos = w.ks + row;
         const float sl2 = a.scale * LOG2E;
         bool ok = true;
         QIter<T> it;
         it.begin(g, w.src, w.ks, w.g * grp, grp);
-        for (int i = 0; i < n; ++i, it.next()) {
-            const int st = i & 1;
-            if (!waitw(BAR(K_SDP), i & 1, wc) || !waitw(BAR(K_QFULL + st), (i >> 1) & 1, wc)) {
+        Ring<K_QST> qr;
+        if (half) qr.next();
+        for (int i = 0; 2 * i + half < ns; ++i, it.next(), qr.next(), qr.next()) {
+            const int qa = it.start() + 64 * half, ql = it.len() - 64 * half;
+            if (!waitw(BAR(K_SDP + half), i & 1, wc) || !waitw(BAR(K_QFULL + qr.st), qr.ph, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t sr[64], pr[64];
-            tmem_ld_x64(tS, sr);
-            tmem_ld_x64(tP, pr);
-            const int qa = it.start(), ql = it.len();
-            // visible query columns c of this tile: c < ql and (not causal or qa + c >= kpos)
-            int lo = 0;
-            if (a.causal) lo = kpos - qa;
-            lo -= 64 * half;
-            const int hi = ql - 64 * half;
-            const float *ls = stat + st * 256 + 64 * half, *dl = ls + 128;
+            tmem_ld2_x64(tb, sr, tb + 64u, pr);
+            // visible query columns c: c < ql and (not causal or qa + c >= kpos)
+            const int lo = a.causal ? kpos - qa : 0;
+            const float4 *ls4 = reinterpret_cast<const float4 *>(stat + qr.st * 128);
+            const float4 *dl4 = ls4 + 16;
             uint32_t pp[32], dd[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int c0 = 2 * e, c1 = 2 * e + 1;
-                const float p0 = ex2(fmaf(__uint_as_float(sr[c0]), sl2, -ls[c0]));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[c1]), sl2, -ls[c1]));
-                const bool v0 = c0 >= lo && c0 < hi, v1 = c1 >= lo && c1 < hi;
-                const float q0 = v0 ? p0 : 0.f, q1 = v1 ? p1 : 0.f;
-                pp[e] = pack_bf16(q0, q1);
-                dd[e] = pack_bf16(q0 * (__uint_as_float(pr[c0]) - dl[c0]),
-                                  q1 * (__uint_as_float(pr[c1]) - dl[c1]));
+            for (int e4 = 0; e4 < 16; ++e4) {
+                const float4 l = ls4[e4], d = dl4[e4];
+                const float lv[4] = {l.x, l.y, l.z, l.w}, dv4[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int u = 0; u < 4; u += 2) {
+                    const int c0 = 4 * e4 + u, c1 = c0 + 1;
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[c0]), sl2, -lv[u]));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[c1]), sl2, -lv[u + 1]));
+                    const bool v0 = c0 >= lo && c0 < ql, v1 = c1 >= lo && c1 < ql;
+                    const float q0 = v0 ? p0 : 0.f, q1 = v1 ? p1 : 0.f;
+                    pp[c0 >> 1] = pack_bf16(q0, q1);
+                    dd[c0 >> 1] = pack_bf16(q0 * (__uint_as_float(pr[c0]) - dv4[u]),
+                                            q1 * (__uint_as_float(pr[c1]) - dv4[u + 1]));
+                }
             }
-            tmem_st_x32(tS, pp);
-            tmem_st_x32(tP, dd);
+            tmem_st_x32(tb, pp);
+            tmem_st_x32(tb + 64u, dd);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(K_PDS));
+            if (lane == 0) mbar_arrive(BAR(K_PDS + half));
         }
         if (ok && waitw(BAR(K_FIN), 0, wc)) {
             tc_fence_after();
             // half 0 writes dV, half 1 writes dK (times scale)
             const bool valid = row < w.kl;
             const float f = half ? a.scale : 1.f;
-            const uint32_t tAcc = tmem + lane_off + (half ? 384u : 256u);
+            const uint32_t tAcc = tmem + lane_off + (half ? C::TM_DK : C::TM_DV);
             __nv_bfloat16 *orow = (half ? dk : dv) + (((int64_t)w.b * a.S + kpos) * a.Hkv + w.g) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -658,9 +808,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D>
 int launch_bwd_d(const BwdPtrs &p, BwdArgs a, cudaStream_t st)
 {
-    CUtensorMap mq, mk, mv, mdo;
-    if (!make_map(&mq, p.q, a.B, a.S, a.Hq, D) || !make_map(&mk, p.k, a.B, a.S, a.Hkv, D) ||
-        !make_map(&mv, p.v, a.B, a.S, a.Hkv, D) || !make_map(&mdo, p.dout, a.B, a.S, a.Hq, D))
+    CUtensorMap mk, mv, mdo, mq64, mdo64;
+    if (!make_map(&mk, p.k, a.B, a.S, a.Hkv, D) || !make_map(&mv, p.v, a.B, a.S, a.Hkv, D) ||
+        !make_map(&mdo, p.dout, a.B, a.S, a.Hq, D) || !make_map(&mq64, p.q, a.B, a.S, a.Hq, D, 64) ||
+        !make_map(&mdo64, p.dout, a.B, a.S, a.Hq, D, 64))
         return CP_ECUDA;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -692,10 +843,11 @@ int launch_bwd_d(const BwdPtrs &p, BwdArgs a, cudaStream_t st)
     const int64_t kunits = (int64_t)g.N * g.cpr * a.tpc * a.B * a.Hkv;
     if (qunits > 0x7fffffffLL || kunits > 0x7fffffffLL) return CP_EUNSUPPORTED;
     bwd_dq_kernel<D><<<(unsigned)qunits, NTHREADS, DqCfg<D>::SMEM, st>>>(
-        mq, mk, mv, mdo, a, p.lse, delta, static_cast<__nv_bfloat16 *>(p.dq));
+        mk, mv, mdo, a, static_cast<const __nv_bfloat16 *>(p.q), p.lse, delta,
+        static_cast<__nv_bfloat16 *>(p.dq));
     if (cudaGetLastError() != cudaSuccess) return CP_ECUDA;
     bwd_dkdv_kernel<D><<<(unsigned)kunits, NTHREADS, DkvCfg<D>::SMEM, st>>>(
-        mq, mk, mv, mdo, a, p.lse, delta, static_cast<__nv_bfloat16 *>(p.dk),
+        mq64, mk, mv, mdo64, a, p.lse, delta, static_cast<__nv_bfloat16 *>(p.dk),
         static_cast<__nv_bfloat16 *>(p.dv));
     return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
 }

@@ -200,14 +200,39 @@ CP_HD Unit decode_unit(const Geom &g, int B, int Hq, int lo, int hi, int upc, in
     return w;
 }
 
+// The same units numbered with each (batch, head) contiguous: all query tiles
+// of one head (by descending position) before the next head.  Blocks that run
+// together then stream the KV tiles of one or two heads, which stay in L2.
+CP_HD Unit decode_unit_grouped(const Geom &g, int B, int Hq, int upc, int qrows, int u)
+{
+    const int nch = num_selected_chunks(g, 0, g.N);
+    Unit w;
+    const int pu = u % upc;
+    int rest = u / upc;
+    const int cu = rest % nch;
+    rest /= nch;
+    w.h = rest % Hq;
+    w.b = rest / Hq;
+    const int ch = selected_chunk(g, 0, g.N, cu);
+    w.r = chunk_rank(g, ch);
+    const int cstart = ch * g.clen;
+    w.cend = cstart + g.clen;
+    w.q0 = cstart + (upc - 1 - pu) * qrows;
+    int last = w.q0 + qrows;
+    if (last > w.cend) last = w.cend;
+    w.qmax = last - 1;
+    return w;
+}
+
 // ---------------------------------------------------------------------------
 // Backward: key-stationary walk.  A KV tile of the shard of rank src receives
 // gradient from the queries of every rank r that holds it at some ring step,
 // r = (src + k) mod N for k = 0..N-1 (the same (rank, step) pairs the forward
 // visits), and from every query head of its GQA group.
 
-// Units of KV tiles: heads fastest, then batch, then tiles by ascending
-// position (under a causal mask early keys receive the most work).
+// Units of KV tiles: tiles by ascending position (under a causal mask early
+// keys receive the most work), then kv head, then batch -- each (batch, kv
+// head) contiguous, so that blocks running together read the same queries.
 struct KvUnit {
     int b, g;       // batch, kv head
     int src;        // rank holding the tile's chunk
@@ -220,12 +245,14 @@ template <int TILE>
 CP_HD KvUnit decode_kv_unit(const Geom &g, int B, int Hkv, int tpc, int u)
 {
     KvUnit w;
-    w.g = u % Hkv;
-    int rest = u / Hkv;
-    w.b = rest % B;
-    rest /= B;
-    const int t = rest % tpc;
-    const int ch = rest / tpc;
+    const int nch = g.N * g.cpr;
+    const int t = u % tpc;
+    int rest = u / tpc;
+    const int ch = rest % nch;
+    rest /= nch;
+    w.g = rest % Hkv;
+    w.b = rest / Hkv;
+    (void)B;
     w.src = chunk_rank(g, ch);
     const int cstart = ch * g.clen;
     w.kcend = cstart + g.clen;
