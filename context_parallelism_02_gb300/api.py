@@ -95,7 +95,8 @@ def ring_attn_bwd_workspace(B: int, Hq: int, S: int) -> int:
 def ring_attn_bwd(q, k, v, out, lse, dout, N: int, layout: int, causal: bool = True,
                   scale: float | None = None, dq=None, dk=None, dv=None, workspace=None,
                   stream=None):
-    """Gradients (dq, dk, dv) of sum(dout * out) for :func:`ring_attn_fwd` (bf16).
+    """Gradients (dq, dk, dv) of sum(dout * out) for :func:`ring_attn_fwd`
+    (bf16 on the tensor cores, or fp32 with fp64 arithmetic).
 
     ``workspace``: optional caller-owned device buffer of at least
     ``ring_attn_bwd_workspace(B, Hq, S)`` bytes (allocated with torch if None).

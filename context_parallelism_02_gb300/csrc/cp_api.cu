@@ -209,7 +209,7 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
     int rc = check_shard(S, N, layout);
     if (rc) return rc;
     if (Hq % Hkv) return CP_EINVAL;
-    if (dtype != CP_BF16) return CP_EUNSUPPORTED;
+    if (dtype != CP_BF16 && dtype != CP_F32) return CP_EUNSUPPORTED;
     if (D != 64 && D != 128) return CP_EUNSUPPORTED;
     if (B == 0 || S == 0) return CP_OK;
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace) return CP_EINVAL;
@@ -235,6 +235,7 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
     a.limit_ns = WAIT_LIMIT_NS;
     if (!a.err) return CP_ECUDA;
     BwdPtrs p{q, k, v, out, lse, dout, dq, dk, dv, workspace};
+    if (dtype == CP_F32) return launch_bwd_f32(p, a, static_cast<cudaStream_t>(stream));
     return launch_bwd_bf16(p, a, static_cast<cudaStream_t>(stream));
 }
 

@@ -37,6 +37,8 @@ struct BwdPtrs {
     void *workspace;   // Delta, bwd_workspace_bytes() bytes
 };
 int launch_bwd_bf16(const BwdPtrs &p, const FwdArgs &a, cudaStream_t st);
+// fp32 inputs/outputs, fp64 arithmetic; does not touch p.workspace
+int launch_bwd_f32(const BwdPtrs &p, const FwdArgs &a, cudaStream_t st);
 size_t bwd_workspace_bytes(int B, int Hq, int64_t S);
 
 // Number of SMs of the current device (cached per device).

@@ -160,13 +160,16 @@ int ulysses_head_to_seq(const void *y, void *x, int B, int64_t S, int H, int D, 
  * step, tile) schedule as the forward:
  *   P = exp(scale q.k - lse), Delta = rowsum(dout * out), dS = P (dout.v - Delta),
  *   dq = scale dS k, dk = scale dS^T q, dv = P^T dout.
- *   q, out, dout, dq [B][S][Hq][D]; k, v, dk, dv [B][S][Hkv][D]: device bf16.
+ *   q, out, dout, dq [B][S][Hq][D]; k, v, dk, dv [B][S][Hkv][D]: device,
+ *   bf16 (dtype CP_BF16: tensor cores, fp32 accumulation) or fp32 (CP_F32:
+ *   the precision path, fp64 arithmetic on the CUDA cores).
  *   lse [B][Hq][S] fp32: the forward's lse (natural log).
  *   workspace: device, at least ring_attn_bwd_workspace(B, Hq, S) bytes,
- *   16-byte aligned, caller-owned scratch (Delta); its contents on entry do
- *   not matter and are overwritten.
+ *   16-byte aligned, caller-owned scratch (Delta, bf16 path; the fp32 path
+ *   forms Delta in fp64 itself and leaves it untouched); its contents on
+ *   entry do not matter and are overwritten.
  *   Every output element is written exactly once (no atomics): the result is
- *   deterministic.  dtype must be CP_BF16; D in {64, 128}.
+ *   deterministic.  D in {64, 128}.
  * Errors: CP_EINVAL (as ring_attn_fwd, plus a null or too small workspace),
  * CP_EUNSUPPORTED (dtype or D), CP_ECUDA.
  */
@@ -185,7 +188,8 @@ size_t ring_attn_bwd_workspace(int B, int Hq, int64_t S);
  * may only use buffers handed to it (a plugin inside another framework, a
  * caller bound to a memory pool or a fixed budget) and so has no way to
  * provide ring_attn_bwd's workspace.  Same arguments, layouts and results as
- * ring_attn_bwd, minus the workspace: the scratch (one fp32 per
+ * ring_attn_bwd with dtype CP_BF16 (the only dtype it takes), minus the
+ * workspace: the scratch (one fp32 per
  * (batch, query head, position)) lives in a 16 MiB array compiled into the
  * library, which every GPU that loads the library keeps until the process
  * exits.  The call allocates nothing.
