@@ -27,7 +27,8 @@ import torch
 
 CONTIGUOUS = 0
 ZIGZAG = 1
-LAYOUT_NAMES = {CONTIGUOUS: "contiguous", ZIGZAG: "zigzag"}
+STRIPED = 2
+LAYOUT_NAMES = {CONTIGUOUS: "contiguous", ZIGZAG: "zigzag", STRIPED: "striped"}
 
 
 @dataclass(frozen=True)

@@ -32,6 +32,7 @@ _lib = None
 
 CONTIGUOUS = 0
 ZIGZAG = 1
+STRIPED = 2
 
 
 def build(force: bool = False) -> str:

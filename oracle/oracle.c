@@ -14,6 +14,8 @@
  *    rescaling equations), "Causal Masking and Load Balancing" (j <= i),
  *    "DeepSpeed Ulysses" (the [Batch, S/P, H, D] <-> [Batch, S, H/P, D]
  *    relayout).
+ *  - the same page, "Causal Masking and Load Balancing" (striped
+ *    partitioning: token t goes to rank t mod P);
  *  - "Context Parallelism" (aiwiki): "The causal imbalance" (zigzag: 2N
  *    chunks, rank i holds chunks i and 2N-1-i), the ring sketch (source rank
  *    = (rank - step) mod world, N compute steps).
@@ -24,6 +26,8 @@
  *  - tensors are BSHD in global token order: q [B][S][Hq][D],
  *    k, v [B][S][Hkv][D]; lse is [B][Hq][rows], natural log;
  *  - query head h uses kv head h / (Hq / Hkv) (contiguous GQA groups);
+ *  - striped: rank r keeps its tokens r, r+N, r+2N, ... in ascending order
+ *    (local row t is position r + N t);
  *  - causal means key j is visible to query i iff j <= i (diagonal included);
  *  - the page's O_block in the rescaling equations is the block's
  *    unnormalised numerator sum_j e^{s_j - m_block} v_j, while O_prev is the
@@ -45,9 +49,20 @@
 
 #define OR_CONTIGUOUS 0
 #define OR_ZIGZAG 1
+#define OR_STRIPED 2
 
 /* ------------------------------------------------------------------------ */
 /* Sequence sharding ("Algorithmic Mechanics" step 1; "The causal imbalance") */
+
+/* Shapes each layout accepts: N ranks of S/N rows; zigzag also needs 2N
+ * equal chunks. */
+static int or_layout_ok(int64_t S, int N, int layout)
+{
+    if (N < 1 || S < 0 || S % N) return 0;
+    if (layout != OR_CONTIGUOUS && layout != OR_ZIGZAG && layout != OR_STRIPED) return 0;
+    if (layout == OR_ZIGZAG && S % (2 * (int64_t)N)) return 0;
+    return 1;
+}
 
 /* Global position of local row t of rank r. */
 static int64_t or_pos(int64_t S, int N, int layout, int r, int64_t t)
@@ -56,6 +71,8 @@ static int64_t or_pos(int64_t S, int N, int layout, int r, int64_t t)
         int64_t blk = S / N;                 /* B = s/P */
         return (int64_t)r * blk + t;
     }
+    if (layout == OR_STRIPED)                /* round robin: position p on rank p mod N */
+        return (int64_t)r + (int64_t)N * t;
     int64_t c = S / (2 * (int64_t)N);        /* 2N chunks */
     if (t < c)
         return (int64_t)r * c + t;           /* chunk r */
@@ -71,8 +88,7 @@ static int or_source(int N, int r, int k)
 
 int or_shard_pos(int64_t S, int N, int layout, int64_t *pos)
 {
-    if (N < 1 || S % N) return -1;
-    if (layout == OR_ZIGZAG && S % (2 * (int64_t)N)) return -1;
+    if (!or_layout_ok(S, N, layout)) return -1;
     int64_t L = S / N;
     for (int r = 0; r < N; ++r)
         for (int64_t t = 0; t < L; ++t)
@@ -93,8 +109,7 @@ int or_ring_source_table(int N, int *src /* [N steps][N ranks] */)
  * key positions j of the source rank with j <= p (all of them if not causal). */
 int or_pair_counts(int64_t S, int N, int layout, int causal, int64_t *counts)
 {
-    if (N < 1 || S % N) return -1;
-    if (layout == OR_ZIGZAG && S % (2 * (int64_t)N)) return -1;
+    if (!or_layout_ok(S, N, layout)) return -1;
     int64_t L = S / N;
     memset(counts, 0, sizeof(int64_t) * (size_t)N * N);
     for (int r = 0; r < N; ++r) {
@@ -182,8 +197,7 @@ int or_ring_fwd(const double *q, const double *k, const double *v,
                 int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout,
                 double scale, double *out, double *lse)
 {
-    if (N < 1 || S % N || Hkv < 1 || Hq % Hkv) return -1;
-    if (layout == OR_ZIGZAG && S % (2 * (int64_t)N)) return -1;
+    if (!or_layout_ok(S, N, layout) || Hkv < 1 || Hq % Hkv) return -1;
     const int grp = Hq / Hkv;
     const int64_t L = S / N;
     int64_t total = (int64_t)B * Hq * S;   /* (b, h, r, t) flattened */
@@ -288,8 +302,7 @@ int or_lse_merge(const double *out_a, const double *lse_a, const double *out_b,
 static int or_ulysses(const unsigned char *x, unsigned char *y, int B, int64_t S, int H, int D,
                       int N, int layout, int elem, int to_head)
 {
-    if (N < 1 || S % N || H % N) return -1;
-    if (layout == OR_ZIGZAG && S % (2 * (int64_t)N)) return -1;
+    if (!or_layout_ok(S, N, layout) || H % N) return -1;
     const int64_t L = S / N;
     const int hg = H / N;
     const size_t row = (size_t)D * elem;

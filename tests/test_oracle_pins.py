@@ -14,7 +14,7 @@ import torch
 from context_parallelism_02_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-CONT, ZIG = 0, 1
+CONT, ZIG, STR = 0, 1, 2
 
 
 def _read_table(name):
@@ -82,7 +82,7 @@ def test_attn_fwd_rows_and_key_range(oracle):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("layout", [CONT, ZIG])
+@pytest.mark.parametrize("layout", [CONT, ZIG, STR])
 @pytest.mark.parametrize("N", [1, 2, 4, 8])
 def test_ring_equals_definition(oracle, N, layout, causal):
     """"Sequence and Context Parallelism", "What it does not change": the
@@ -103,7 +103,7 @@ def test_ring_tiny_workload_all_variants(oracle):
         q, k, v = inputs.make_qkv(w.with_(q_scale=qscale))
         for causal in (True, False):
             ref, lref = oracle.attn_fwd(q, k, v, causal)
-            for layout in (CONT, ZIG):
+            for layout in (CONT, ZIG, STR):
                 o, l = oracle.ring_fwd(q, k, v, w.N, layout, causal)
                 assert np.max(np.abs(o - ref)) < 1e-12
                 assert np.max(np.abs(l - lref)) < 1e-11
@@ -127,7 +127,7 @@ def test_row_sums(oracle, causal):
 # ---------------------------------------------------------------- (d) constant V
 
 
-@pytest.mark.parametrize("layout", [CONT, ZIG])
+@pytest.mark.parametrize("layout", [CONT, ZIG, STR])
 def test_constant_v(oracle, layout):
     S, D = 64, 16
     q, k = _rand((1, S, 2, D), 13), _rand((1, S, 2, D), 14)
@@ -155,11 +155,23 @@ def _brute_counts(pos, causal):
 
 
 @pytest.mark.parametrize("S,N", [(32, 4), (48, 2), (64, 8), (40, 1)])
-@pytest.mark.parametrize("layout", [CONT, ZIG])
+@pytest.mark.parametrize("layout", [CONT, ZIG, STR])
 @pytest.mark.parametrize("causal", [True, False])
 def test_pair_counts_brute_force(oracle, S, N, layout, causal):
-    pos = np.arange(S).reshape(N, S // N) if layout == CONT else _zigzag_pos(S, N)
-    np.testing.assert_array_equal(oracle.pair_counts(S, N, layout, causal), _brute_counts(pos, causal))
+    np.testing.assert_array_equal(oracle.pair_counts(S, N, layout, causal),
+                                  _brute_counts(_page_pos(S, N, layout), causal))
+
+
+def _striped_pos(S, N):
+    """"Causal Masking and Load Balancing": token t goes to rank t mod P; a
+    rank keeps its tokens in sequence order."""
+    return np.array([[p for p in range(S) if p % N == r] for r in range(N)])
+
+
+def _page_pos(S, N, layout):
+    if layout == CONT:
+        return np.arange(S).reshape(N, S // N)
+    return _zigzag_pos(S, N) if layout == ZIG else _striped_pos(S, N)
 
 
 def _zigzag_pos(S, N):
@@ -196,6 +208,26 @@ def test_pair_count_closed_forms(oracle, S, N):
     assert np.all(nc == C * C)
 
 
+@pytest.mark.parametrize("S,N", [(512, 4), (8192, 8), (1024, 16), (96, 3)])
+def test_striped_pair_count_closed_forms(oracle, S, N):
+    """Striped partitioning ("Causal Masking and Load Balancing"): with C = S/N
+    rows per rank, query r + N t sees the keys src + N u with u <= t - [src > r],
+    so step k (src = (r - k) mod N) has C(C+1)/2 - C [src > r] pairs, rank r
+    in total N C(C+1)/2 - C (N - 1 - r): every rank within C(N-1) pairs of
+    every other ("equal causal density"), summing to S(S+1)/2."""
+    C = S // N
+    st = oracle.pair_counts(S, N, STR, True)
+    for r in range(N):
+        for kk in range(N):
+            src = (r - kk) % N
+            assert st[r, kk] == C * (C + 1) // 2 - (C if src > r else 0)
+        assert st[r].sum() == N * C * (C + 1) // 2 - C * (N - 1 - r)
+    assert st.sum() == S * (S + 1) // 2
+    tot = st.sum(1)
+    assert tot.max() - tot.min() == C * (N - 1)
+    assert np.all(oracle.pair_counts(S, N, STR, False) == C * C)
+
+
 def test_pair_counts_imbalance_example(oracle):
     """The worked example (S=8192, N=8): rank 0 attends to almost nothing,
     rank 7 to everything; zigzag makes every rank equal."""
@@ -221,6 +253,11 @@ def test_shard_map_golden(oracle):
                                                              np.arange(b * c, b * c + c)]))
     # every position appears exactly once
     assert sorted(pz.reshape(-1).tolist()) == list(range(S))
+    # striped: rank p mod N holds position p
+    for S, N in ((64, 4), (96, 3), (40, 8), (7, 1)):
+        ps = oracle.shard_pos(S, N, STR)
+        np.testing.assert_array_equal(ps, _striped_pos(S, N))
+        assert sorted(ps.reshape(-1).tolist()) == list(range(S))
 
 
 def test_ring_schedule_golden(oracle):
@@ -293,7 +330,7 @@ def test_merge_closed_form_equal_lse(oracle):
 # ---------------------------------------------------------------- (h) Ulysses relayout
 
 
-@pytest.mark.parametrize("layout", [CONT, ZIG])
+@pytest.mark.parametrize("layout", [CONT, ZIG, STR])
 @pytest.mark.parametrize("N,H", [(2, 4), (4, 8), (8, 8), (1, 3)])
 def test_ulysses_against_slicing(oracle, N, H, layout):
     """"DeepSpeed Ulysses": rank g ends with the full sequence for heads
@@ -303,7 +340,7 @@ def test_ulysses_against_slicing(oracle, N, H, layout):
     y = oracle.ulysses_seq_to_head(x, N, layout)
     # global tensor assembled with numpy from the page's chunk definition
     xs = x.view(torch.int16).numpy()
-    pos = np.arange(S).reshape(N, S // N) if layout == CONT else _zigzag_pos(S, N)
+    pos = _page_pos(S, N, layout)
     glob = np.zeros((B, S, H, D), np.int16)
     for r in range(N):
         glob[:, pos[r]] = xs[r]
@@ -394,3 +431,7 @@ def test_oracle_rejects_bad_shapes(oracle):
         oracle.shard_pos(12, 4, ZIG)
     with pytest.raises(ValueError):
         oracle.pair_counts(12, 4, ZIG, True)
+    with pytest.raises(ValueError):
+        oracle.shard_pos(12, 5, STR)
+    with pytest.raises(ValueError):
+        oracle.shard_pos(12, 4, 3)
