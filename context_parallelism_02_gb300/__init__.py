@@ -5,6 +5,7 @@ include/cp.h); this package only loads it and marshals arguments.
 """
 from . import api, inputs  # noqa: F401
 from ._lib import (CP_BF16, CP_EHEADS, CP_EINVAL, CP_ETIMEOUT, CP_EUNSUPPORTED, CP_F32,  # noqa: F401
-                   CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_ZIGZAG, CP_OK, CpError)
+                   CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIPED, CP_LAYOUT_ZIGZAG, CP_OK,
+                   CpError)
 
 __all__ = ["api", "inputs", "CpError"]

@@ -20,6 +20,7 @@ CP_ETIMEOUT = -5
 
 CP_LAYOUT_CONTIGUOUS = 0
 CP_LAYOUT_ZIGZAG = 1
+CP_LAYOUT_STRIPED = 2
 CP_F32 = 0
 CP_BF16 = 1
 CP_BWD_NOALLOC_MAX_ROWS = 4 * 1024 * 1024

@@ -286,8 +286,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j >= Q_KST && !wait1(BAR(Q_KEMPTY + kr.st), kr.ph ^ 1, wc)) break;
                 mbar_arrive_expect_tx(BAR(Q_KFULL + kr.st), TB);
                 for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load4(sK + kr.st * TB + bx * 16384, &tmK, BAR(Q_KFULL + kr.st), bx * 64, kvh,
-                              it.start(), w.b, pol_kv);
+                    tma_load5(sK + kr.st * TB + bx * 16384, &tmK, BAR(Q_KFULL + kr.st), bx * 64, kvh,
+                              it.mrank(), it.mrow(), w.b, pol_kv);
                 ++nk;
             }
             if (*abort_flag) {
@@ -302,7 +302,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
             mbar_arrive_expect_tx(BAR(Q_DOFULL), TB);
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load4(sDO + bx * 16384, &tmDO, BAR(Q_DOFULL), bx * 64, w.h, w.q0, w.b, pol_q);
+                tma_load5(sDO + bx * 16384, &tmDO, BAR(Q_DOFULL), bx * 64, w.h, slot_mrank(g, w.q0),
+                          slot_mrow(g, w.q0), w.b, pol_q);
             KvIter<T> it;
             it.begin(g, w.r, w.qmax);
             int nv = 0;
@@ -311,8 +312,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j >= 2 && !wait1(BAR(Q_VEMPTY + sv), ((j >> 1) - 1) & 1, wc)) break;
                 mbar_arrive_expect_tx(BAR(Q_VFULL + sv), TB);
                 for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load4(sV + sv * TB + bx * 16384, &tmV, BAR(Q_VFULL + sv), bx * 64, kvh,
-                              it.start(), w.b, pol_kv);
+                    tma_load5(sV + sv * TB + bx * 16384, &tmV, BAR(Q_VFULL + sv), bx * 64, kvh,
+                              it.mrank(), it.mrow(), w.b, pol_kv);
                 ++nv;
             }
             if (*abort_flag) {
@@ -390,7 +391,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tP = tmem + lane_off + C::TM_P + 64u * half;
         const uint32_t tDQ = tmem + lane_off + C::TM_DQ;
         const uint32_t tDS = tmem + lane_off + C::TM_DS + 32u * half;
-        const int qpos = w.q0 + row;
+        const int qpos = w.q0 + row;                  // slot
+        const int qp = slot_pos(g, qpos);             // global position
         const bool valid = qpos < w.cend;
         {
             // this half's D/2 elements of the Q row, as D/4 bf16 pairs (rows past the
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t qv[D / 4];
             if (valid) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
-                    q + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D + (D / 2) * half);
+                    q + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D + (D / 2) * half);
 #pragma unroll
                 for (int i = 0; i < D / 16; ++i) {
                     const uint4 x = src[i];
@@ -422,8 +424,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float sl2 = a.scale * LOG2E;
         float lse2 = 0.f, dlt = 0.f;
         if (valid) {
-            lse2 = lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] * LOG2E;
-            dlt = delta[((int64_t)w.b * a.Hq + w.h) * a.S + qpos];
+            lse2 = lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] * LOG2E;
+            dlt = delta[((int64_t)w.b * a.Hq + w.h) * a.S + qp];
         }
         bool ok = true;
         KvIter<T> it;
@@ -432,7 +434,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int ks = it.start(), kl = it.len();
             int lim = kl;                              // visible columns [0, lim) of the tile
             if (a.causal) {
-                const int c = qpos - ks + 1;
+                const int c = qpos - ks + 1 + it.shift;
                 lim = c < lim ? c : lim;
             }
             lim -= 64 * half;                          // in this half's local columns
@@ -481,7 +483,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
             // each half writes D/2 columns of dQ = scale * acc
             constexpr int HD = D / 2;
-            __nv_bfloat16 *orow = dq + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D + HD * half;
+            __nv_bfloat16 *orow = dq + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D + HD * half;
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
@@ -618,8 +620,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(K_KVFULL), 2 * TB);
                 for (int bx = 0; bx < D / 64; ++bx) {
-                    tma_load4(sK + bx * 16384, &tmK, BAR(K_KVFULL), bx * 64, w.g, w.ks, w.b, pol_kv);
-                    tma_load4(sV + bx * 16384, &tmV, BAR(K_KVFULL), bx * 64, w.g, w.ks, w.b, pol_kv);
+                    tma_load5(sK + bx * 16384, &tmK, BAR(K_KVFULL), bx * 64, w.g, slot_mrank(g, w.ks),
+                              slot_mrow(g, w.ks), w.b, pol_kv);
+                    tma_load5(sV + bx * 16384, &tmV, BAR(K_KVFULL), bx * 64, w.g, slot_mrank(g, w.ks),
+                              slot_mrow(g, w.ks), w.b, pol_kv);
                 }
             }
             QIter<T> it;
@@ -630,12 +634,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (s >= K_QST && !waitw(BAR(K_QEMPTY + qr.st), qr.ph ^ 1, wc)) break;
                 const int hs = s & 1;
                 const int qa = it.start() + 64 * hs, ql = it.len() - 64 * hs, h = it.head();
+                const int qr_rank = it.mrank(), qr_row = it.mrow() + 64 * hs;   // map coordinates
                 // per-row statistics of the half tile: lse (log2 units) and Delta
                 float *ls = stat + qr.st * 128, *dl = ls + 64;
                 for (int e = lane; e < 64; e += 32) {
                     float l2 = 0.f, dd = 0.f;
                     if (e < ql) {
-                        const int64_t off = ((int64_t)w.b * a.Hq + h) * a.S + qa + e;
+                        const int64_t off = ((int64_t)w.b * a.Hq + h) * a.S + slot_pos(g, qa + e);
                         l2 = lse[off] * LOG2E;
                         dd = delta[off];
                     }
@@ -647,9 +652,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t sq = sQ + qr.st * C::STAGE;
                     mbar_arrive_expect_tx(BAR(K_QFULL + qr.st), 2 * HB);
                     for (int bx = 0; bx < D / 64; ++bx) {
-                        tma_load4(sq + bx * 8192, &tmQh, BAR(K_QFULL + qr.st), bx * 64, h, qa, w.b, pol_q);
-                        tma_load4(sq + HB + bx * 8192, &tmDOh, BAR(K_QFULL + qr.st), bx * 64, h, qa, w.b,
-                                  pol_q);
+                        tma_load5(sq + bx * 8192, &tmQh, BAR(K_QFULL + qr.st), bx * 64, h, qr_rank,
+                                  qr_row, w.b, pol_q);
+                        tma_load5(sq + HB + bx * 8192, &tmDOh, BAR(K_QFULL + qr.st), bx * 64, h, qr_rank,
+                                  qr_row, w.b, pol_q);
                     }
                 }
                 __syncwarp();
@@ -736,7 +742,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Ring<K_QST> qr;
         if (half) qr.next();
         for (int i = 0; 2 * i + half < ns; ++i, it.next(), qr.next(), qr.next()) {
-            const int qa = it.start() + 64 * half, ql = it.len() - 64 * half;
+            const int qa = it.start() + 64 * half, ql = it.len() - 64 * half, sh = it.shift;
             if (!waitw(BAR(K_SDP + half), i & 1, wc) || !waitw(BAR(K_QFULL + qr.st), qr.ph, wc)) {
                 ok = false;
                 break;
@@ -745,7 +751,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t sr[64], pr[64];
             tmem_ld2_x64(tb, sr, tb + 64u, pr);
             // visible query columns c: c < ql and (not causal or qa + c >= kpos)
-            const int lo = a.causal ? kpos - qa : 0;
+            const int lo = a.causal ? kpos - sh - qa : 0;
             const float4 *ls4 = reinterpret_cast<const float4 *>(stat + qr.st * 128);
             const float4 *dl4 = ls4 + 16;
             uint32_t pp[32], dd[32];
@@ -778,7 +784,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const bool valid = row < w.kl;
             const float f = half ? a.scale : 1.f;
             const uint32_t tAcc = tmem + lane_off + (half ? C::TM_DK : C::TM_DV);
-            __nv_bfloat16 *orow = (half ? dk : dv) + (((int64_t)w.b * a.S + kpos) * a.Hkv + w.g) * D;
+            __nv_bfloat16 *orow = (half ? dk : dv) + (((int64_t)w.b * a.S + slot_pos(g, kpos)) * a.Hkv + w.g) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -809,9 +815,10 @@ template <int D>
 int launch_bwd_d(const BwdPtrs &p, BwdArgs a, cudaStream_t st)
 {
     CUtensorMap mk, mv, mdo, mq64, mdo64;
-    if (!make_map(&mk, p.k, a.B, a.S, a.Hkv, D) || !make_map(&mv, p.v, a.B, a.S, a.Hkv, D) ||
-        !make_map(&mdo, p.dout, a.B, a.S, a.Hq, D) || !make_map(&mq64, p.q, a.B, a.S, a.Hq, D, 64) ||
-        !make_map(&mdo64, p.dout, a.B, a.S, a.Hq, D, 64))
+    const int R = a.layout == CP_LAYOUT_STRIPED ? a.N : 1;
+    if (!make_map(&mk, p.k, a.B, a.S, a.Hkv, D, 128, R) || !make_map(&mv, p.v, a.B, a.S, a.Hkv, D, 128, R) ||
+        !make_map(&mdo, p.dout, a.B, a.S, a.Hq, D, 128, R) ||
+        !make_map(&mq64, p.q, a.B, a.S, a.Hq, D, 64, R) || !make_map(&mdo64, p.dout, a.B, a.S, a.Hq, D, 64, R))
         return CP_ECUDA;
     static bool attr_done[64] = {};
     int dev = 0;

@@ -70,12 +70,13 @@ __global__ void __launch_bounds__(WARPS * 32)
     const int kvh = w.h / (a.Hq / a.Hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = warp;
-    const int qpos = w.q0 + row;
+    const int qpos = w.q0 + row;              // slot
+    const int qp = slot_pos(g, qpos);         // global position
     const bool valid = qpos < w.cend;
 
     // the warp's query row, and Delta = rowsum(dO * out) in fp64
     double dlt = 0.0;
-    const int64_t roff = (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D;
+    const int64_t roff = (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) {
         const int d = lane + 32 * e;
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         dlt = fma((double)gv, (double)ov, dlt);
     }
     dlt = warp_sum(dlt);
-    const double lse_i = valid ? (double)lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] : 0.0;
+    const double lse_i = valid ? (double)lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] : 0.0;
 
     double acc[DPL];
 #pragma unroll
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(WARPS * 32)
             const int j = i / D, d = i % D;
             float kv = 0.f, vv = 0.f;
             if (j < kl) {
-                const int64_t off = (((int64_t)w.b * a.S + ks + j) * a.Hkv + kvh) * D + d;
+                const int64_t off = (((int64_t)w.b * a.S + slot_pos(g, ks + j)) * a.Hkv + kvh) * D + d;
                 kv = k[off];
                 vv = v[off];
             }
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         __syncthreads();
         // lane j: dS of (row, key j)
         double ds = 0.0;
-        if (valid && lane < kl && (!a.causal || ks + lane <= qpos)) {
+        if (valid && lane < kl && (!a.causal || ks + lane <= qpos + it.shift)) {
             double s = 0.0, dp = 0.0;
 #pragma unroll 8
             for (int d = 0; d < D; ++d) {
@@ -163,9 +164,9 @@ __global__ void __launch_bounds__(WARPS * 32)
     const int grp = a.Hq / a.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = warp;                 // the warp's key row
-    const int kpos = w.ks + j;
+    const int kpos = w.ks + j;   // slot
     const bool kvalid = j < w.kl;
-    const int64_t koff = (((int64_t)w.b * a.S + kpos) * a.Hkv + w.g) * D;
+    const int64_t koff = (((int64_t)w.b * a.S + slot_pos(g, kpos)) * a.Hkv + w.g) * D;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) {
         const int d = lane + 32 * e;
@@ -185,7 +186,8 @@ __global__ void __launch_bounds__(WARPS * 32)
         for (int rr = 0; rr < RPW; ++rr) {
             const int c = warp * RPW + rr;
             const bool cv = c < ql;
-            const int64_t off = (((int64_t)w.b * a.S + qa + c) * a.Hq + h) * D;
+            const int qc = cv ? slot_pos(g, qa + c) : 0;
+            const int64_t off = (((int64_t)w.b * a.S + qc) * a.Hq + h) * D;
             double dl = 0.0;
 #pragma unroll
             for (int e = 0; e < DPL; ++e) {
@@ -203,13 +205,13 @@ __global__ void __launch_bounds__(WARPS * 32)
             dl = warp_sum(dl);
             if (lane == 0) {
                 dlts[c] = dl;
-                lses[c] = cv ? (double)lse[((int64_t)w.b * a.Hq + h) * a.S + qa + c] : 0.0;
+                lses[c] = cv ? (double)lse[((int64_t)w.b * a.Hq + h) * a.S + qc] : 0.0;
             }
         }
         __syncthreads();
         // lane c: P and dS of (query c, key j)
         double p = 0.0, ds = 0.0;
-        if (kvalid && lane < ql && (!a.causal || qa + lane >= kpos)) {
+        if (kvalid && lane < ql && (!a.causal || qa + lane >= kpos - it.shift)) {
             double s = 0.0, dp = 0.0;
 #pragma unroll 8
             for (int d = 0; d < D; ++d) {

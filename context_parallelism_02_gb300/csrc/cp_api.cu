@@ -41,7 +41,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 int check_shard(int64_t S, int N, int layout)
 {
     if (N < 1 || S < 0 || S > 0x7fffffffLL) return CP_EINVAL;
-    if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_ZIGZAG) return CP_EINVAL;
+    if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_ZIGZAG && layout != CP_LAYOUT_STRIPED)
+        return CP_EINVAL;
     if (S % N) return CP_EINVAL;
     if (layout == CP_LAYOUT_ZIGZAG && S % (2 * (int64_t)N)) return CP_EINVAL;
     return CP_OK;
@@ -169,7 +170,9 @@ int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_h
                 int64_t qb = qa + 128;                         // queries [qa, qb)
                 if (qb > w.cend) qb = w.cend;
                 if (qa >= qb) continue;
-                const int64_t p = causal ? visible_pairs(qa, qb, ks, ke - ks) : (qb - qa) * (ke - ks);
+                // in slots the causal diagonal moves by it.shift (striped)
+                const int64_t p = causal ? visible_pairs(qa, qb, ks - it.shift, ke - ks)
+                                         : (qb - qa) * (ke - ks);
                 pairs_host[w.r * N + it.k] += p;
                 if (tiles_host) tiles_host[w.r * N + it.k] += 1;
             }

@@ -6,7 +6,20 @@
 // RingAttention", "Algorithmic Mechanics" step 1; "Context Parallelism",
 // "The causal imbalance"): the sequence is cut into chunks of equal length.
 // Contiguous: N chunks, rank r holds chunk r.  Zigzag: 2N chunks, rank r holds
-// chunks r and 2N-1-r (chunk r first in its local order).
+// chunks r and 2N-1-r (chunk r first in its local order).  Striped ("Causal
+// Masking and Load Balancing", striped partitioning): token p goes to rank
+// p mod N, so rank r holds positions r, r+N, r+2N, ... in that order.
+//
+// Slots: every layout numbers the rows of the ranks' shards 0..S-1, chunk by
+// chunk (chunk ch covers slots [ch*clen, (ch+1)*clen)).  For contiguous and
+// zigzag a slot is its global position.  For striped, chunk r is rank r's
+// whole shard and slot r*clen + t is position r + N t.  The kernels tile
+// slots; the causal test "key position <= query position" between a query
+// chunk of rank r and a key chunk of rank src reads, in slots,
+//   key slot <= query slot + diag_shift(r, src),
+// with diag_shift = 0 for contiguous and zigzag and (src-r)*clen - [src > r]
+// for striped (key row t_k of src is visible to query row t_q of r iff
+// t_k <= t_q - [src > r]).
 //
 // Ring schedule ("Algorithmic Mechanics" step 2; the ring sketch of "Context
 // Parallelism"): at step k = 0..N-1 rank r holds the KV shard of rank
@@ -58,6 +71,28 @@ CP_HD Geom make_geom(int S, int N, int layout, int causal)
     return g;
 }
 
+CP_HD bool striped(const Geom &g) { return g.layout == CP_LAYOUT_STRIPED; }
+
+// Global position of slot u.
+CP_HD int slot_pos(const Geom &g, int u)
+{
+    if (!striped(g)) return u;
+    const int r = u / g.clen;
+    return r + g.N * (u - r * g.clen);
+}
+
+// Causal diagonal between query rank r and key rank src, in slots.
+CP_HD int diag_shift(const Geom &g, int r, int src)
+{
+    if (!striped(g) || !g.causal) return 0;
+    return (src - r) * g.clen - (src > r ? 1 : 0);
+}
+
+// Coordinates of slot u in the tensor maps (rank, row): a striped shard is
+// read with a row stride of N positions, every other layout as one block.
+CP_HD int slot_mrank(const Geom &g, int u) { return striped(g) ? u / g.clen : 0; }
+CP_HD int slot_mrow(const Geom &g, int u) { return striped(g) ? u - (u / g.clen) * g.clen : u; }
+
 // i-th chunk (0 or 1) held by rank r.
 CP_HD int rank_chunk(const Geom &g, int r, int i)
 {
@@ -73,6 +108,7 @@ CP_HD int chunk_rank(const Geom &g, int ch)
 // Global position of local row t of rank r.
 CP_HD int shard_pos(const Geom &g, int r, int t)
 {
+    if (striped(g)) return r + g.N * t;
     int i = t / g.clen;
     return rank_chunk(g, r, i) * g.clen + (t - i * g.clen);
 }
@@ -97,7 +133,7 @@ CP_HD int selected_chunk(const Geom &g, int lo, int hi, int idx)
 }
 
 // Number of TILE-key tiles of chunk [cstart, cstart+clen) that a unit whose
-// last query is qmax must visit.
+// last query slot is qmax must visit (qmax already moved by diag_shift).
 template <int TILE>
 CP_HD int tiles_needed(const Geom &g, int cstart, int qmax)
 {
@@ -117,6 +153,7 @@ struct KvIter {
     int r, qmax;
     int k, ci;
     int t, nt, cstart, cend;
+    int src, shift;     // rank holding the current chunk; diag_shift(r, src)
 
     CP_HD void begin(const Geom &g_, int r_, int qmax_)
     {
@@ -125,7 +162,7 @@ struct KvIter {
         qmax = qmax_;
         k = 0;
         ci = -1;
-        t = nt = cstart = cend = 0;
+        t = nt = cstart = cend = src = shift = 0;
         advance_chunk();
     }
     CP_HD bool advance_chunk()
@@ -137,17 +174,21 @@ struct KvIter {
                 ++k;
             }
             if (k >= g.N) return false;
-            int src = ring_source(g.N, r, k);
+            src = ring_source(g.N, r, k);
+            shift = diag_shift(g, r, src);
             int ch = rank_chunk(g, src, ci);
             cstart = ch * g.clen;
             cend = cstart + g.clen;
-            nt = tiles_needed<TILE>(g, cstart, qmax);
+            nt = tiles_needed<TILE>(g, cstart, qmax + shift);
             t = 0;
             if (nt > 0) return true;
         }
     }
     CP_HD bool valid() const { return k < g.N; }
     CP_HD int start() const { return cstart + t * TILE; }
+    // tensor-map coordinates of the tile's first key
+    CP_HD int mrank() const { return striped(g) ? src : 0; }
+    CP_HD int mrow() const { return striped(g) ? t * TILE : start(); }
     CP_HD int len() const
     {
         int l = cend - start();
@@ -164,7 +205,8 @@ struct KvIter {
         for (int k = 0; k < g.N; ++k) {
             int src = ring_source(g.N, r, k);
             for (int ci = 0; ci < g.cpr; ++ci)
-                n += tiles_needed<TILE>(g, rank_chunk(g, src, ci) * g.clen, qmax);
+                n += tiles_needed<TILE>(g, rank_chunk(g, src, ci) * g.clen,
+                                        qmax + diag_shift(g, r, src));
         }
         return n;
     }
@@ -175,9 +217,9 @@ struct KvIter {
 // descending position.
 struct Unit {
     int b, h, r;
-    int q0;     // first query position
+    int q0;     // first query slot
     int cend;   // end of the unit's chunk (rows at or past it are not stored)
-    int qmax;   // last valid query position
+    int qmax;   // last valid query slot
 };
 
 CP_HD Unit decode_unit(const Geom &g, int B, int Hq, int lo, int hi, int upc, int qrows, int u)
@@ -262,8 +304,8 @@ CP_HD KvUnit decode_kv_unit(const Geom &g, int B, int Hkv, int tpc, int u)
     return w;
 }
 
-// Number of TILE-row query tiles of chunk [cstart, cend) that see key ks, and
-// the first of them.
+// Number of TILE-row query tiles of chunk [cstart, cend) that see key slot ks
+// (already moved by -diag_shift), and the first of them.
 template <int TILE>
 CP_HD int qtiles_seeing(const Geom &g, int cstart, int ks, int &t0)
 {
@@ -281,6 +323,7 @@ struct QIter {
     Geom g;
     int src, ks, h0, grp;
     int hh, k, ci, t, t0, nt, cstart, cend;
+    int r, shift;       // rank of the current query chunk; diag_shift(r, src)
 
     CP_HD void begin(const Geom &g_, int src_, int ks_, int h0_, int grp_)
     {
@@ -292,7 +335,7 @@ struct QIter {
         hh = 0;
         k = 0;
         ci = -1;
-        t = nt = t0 = cstart = cend = 0;
+        t = nt = t0 = cstart = cend = r = shift = 0;
         advance_chunk();
     }
     CP_HD bool advance_chunk()
@@ -308,11 +351,12 @@ struct QIter {
                 }
             }
             if (hh >= grp) return false;
-            const int r = (src + k) % g.N;
+            r = (src + k) % g.N;
+            shift = diag_shift(g, r, src);
             const int ch = rank_chunk(g, r, ci);
             cstart = ch * g.clen;
             cend = cstart + g.clen;
-            nt = qtiles_seeing<TILE>(g, cstart, ks, t0);
+            nt = qtiles_seeing<TILE>(g, cstart, ks - shift, t0);
             t = 0;
             if (nt > 0) return true;
         }
@@ -320,6 +364,9 @@ struct QIter {
     CP_HD bool valid() const { return hh < grp; }
     CP_HD int head() const { return h0 + hh; }
     CP_HD int start() const { return cstart + (t0 + t) * TILE; }
+    // tensor-map coordinates of the tile's first query
+    CP_HD int mrank() const { return striped(g) ? r : 0; }
+    CP_HD int mrow() const { return striped(g) ? (t0 + t) * TILE : start(); }
     CP_HD int len() const
     {
         const int l = cend - start();
@@ -336,7 +383,8 @@ struct QIter {
             const int r = (src + k) % g.N;
             for (int ci = 0; ci < g.cpr; ++ci) {
                 int t0;
-                n += qtiles_seeing<TILE>(g, rank_chunk(g, r, ci) * g.clen, ks, t0);
+                n += qtiles_seeing<TILE>(g, rank_chunk(g, r, ci) * g.clen,
+                                         ks - diag_shift(g, r, src), t0);
             }
         }
         return n * grp;

@@ -191,30 +191,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
             mbar_arrive_expect_tx(BAR(B_Q), C::QBYTES);
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load4(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, w.h, w.q0, w.b, pol_q);
+                tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, w.h, slot_mrank(g, w.q0),
+                          slot_mrow(g, w.q0), w.b, pol_q);
             // K runs one tile ahead of V; the V loads reuse the K tile starts
             KvIter<KT> itk;
             itk.begin(g, w.r, w.qmax);
             int nk = 0, nv = 0;   // tiles whose K / V loads were issued
-            int ks_cur = 0, ks_next = 0;
+            int kr_cur = 0, kw_cur = 0, kr_next = 0, kw_next = 0;   // map coordinates (rank, row)
             bool ok = true;
             auto load_k = [&](int j) -> bool {
                 const int st = j & 1;
                 if (j >= 2 && !wait1(BAR(B_KEMPTY + st), ((j >> 1) - 1) & 1, wc)) return false;
                 mbar_arrive_expect_tx(BAR(B_KFULL + st), C::KBYTES);
-                ks_next = itk.start();
+                kr_next = itk.mrank();
+                kw_next = itk.mrow();
                 for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load4(sK + st * C::KBYTES + bx * C::KBOX, &tmK, BAR(B_KFULL + st), bx * 64,
-                              kvh, ks_next, w.b, pol_kv);
+                    tma_load5(sK + st * C::KBYTES + bx * C::KBOX, &tmK, BAR(B_KFULL + st), bx * 64,
+                              kvh, kr_next, kw_next, w.b, pol_kv);
                 itk.next();
                 ++nk;
                 return true;
             };
             if (n > 0) ok = load_k(0);
             for (int j = 0; ok && j < n; ++j) {
-                ks_cur = ks_next;
+                kr_cur = kr_next;
+                kw_cur = kw_next;
                 if (j + 1 < n && !load_k(j + 1)) break;
-                const int ks = ks_cur;
                 for (int hh = 0; hh < 2; ++hh) {
                     if (j >= 1 && !wait1(BAR(B_VEMPTY + hh), (j - 1) & 1, wc)) {
                         ok = false;
@@ -222,8 +224,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     mbar_arrive_expect_tx(BAR(B_VFULL + hh), C::VBYTES);
                     for (int bx = 0; bx < D / 64; ++bx)
-                        tma_load4(sV + hh * C::VBYTES + bx * 16384, &tmV, BAR(B_VFULL + hh), bx * 64,
-                                  kvh, ks + 128 * hh, w.b, pol_kv);
+                        tma_load5(sV + hh * C::VBYTES + bx * 16384, &tmV, BAR(B_VFULL + hh), bx * 64,
+                                  kvh, kr_cur, kw_cur + 128 * hh, w.b, pol_kv);
                     nv = 2 * j + hh + 1;
                 }
             }
@@ -331,11 +333,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float *s = reinterpret_cast<float *>(sr);
             const int ks = it.start();
             const int kl = it.len();
-            if (kl < KT || (a.causal && ks + kl - 1 > w.q0)) {
+            if (kl < KT || (a.causal && ks + kl - 1 > w.q0 + it.shift)) {
                 // partial tile: key columns [0, lim) of the 256 are visible to this row
                 int lim = kl;
                 if (a.causal) {
-                    const int c = qpos - ks + 1;
+                    const int c = qpos - ks + 1 + it.shift;
                     lim = c < lim ? c : lim;
                 }
                 lim -= 128 * half;
@@ -390,9 +392,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float x0, x1;
                 ffma2(x0, x1, s[c], s[c + 1], sl2, -mu);
                 const float p0 = ex2(x0), p1 = ex2(x1);
+                const uint32_t pk = pack_bf16(p0, p1);
                 fadd2(l0, l1, p0, p1);
-                if (c < 64) pk0[c / 2] = pack_bf16(p0, p1);
-                else pk1[(c - 64) / 2] = pack_bf16(p0, p1);
+                if (c < 64) pk0[c / 2] = pk;
+                else pk1[(c - 64) / 2] = pk;
             }
             if (!early) {
                 if (!waitw(BAR(B_MX), j & 1, wc)) {
@@ -451,7 +454,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float l_tot = pmn[row] + pmn[128 + row];
             const bool valid = qpos < w.cend;
             const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-            __nv_bfloat16 *orow = out + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D + (D / 2) * half;
+            const int qp = slot_pos(g, qpos);   // global position of the row
+            __nv_bfloat16 *orow = out + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D + (D / 2) * half;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             if (ok && valid && half == 0)
-                lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] =
+                lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] =
                     l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
         }
         __syncwarp();
@@ -488,8 +492,9 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
              cudaStream_t st)
 {
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, a.B, a.S, a.Hq, D) || !make_map(&mk, k, a.B, a.S, a.Hkv, D, KT) ||
-        !make_map(&mv, v, a.B, a.S, a.Hkv, D))
+    const int R = a.layout == CP_LAYOUT_STRIPED ? a.N : 1;
+    if (!make_map(&mq, q, a.B, a.S, a.Hq, D, 128, R) || !make_map(&mk, k, a.B, a.S, a.Hkv, D, KT, R) ||
+        !make_map(&mv, v, a.B, a.S, a.Hkv, D, 128, R))
         return CP_ECUDA;
     static bool attr_done[64] = {};
     int dev = 0;

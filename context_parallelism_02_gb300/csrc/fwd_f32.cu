@@ -49,8 +49,8 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
     // load the query rows of the unit (rows past the chunk end are zero)
     for (int i = threadIdx.x; i < QR * D; i += blockDim.x) {
         int rr = i / D, d = i % D;
-        int pos = w.q0 + rr;
-        Qs[rr][d] = (pos < w.cend) ? q[(((int64_t)w.b * a.S + pos) * a.Hq + w.h) * D + d] : 0.f;
+        int pos = w.q0 + rr;   // slot; its global position is slot_pos
+        Qs[rr][d] = (pos < w.cend) ? q[(((int64_t)w.b * a.S + slot_pos(g, pos)) * a.Hq + w.h) * D + d] : 0.f;
     }
 
     double o[ROWS_PER_WARP][DPL];
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
             int j = i / D, d = i % D;
             float kv = 0.f, vv = 0.f;
             if (j < kl) {
-                int64_t off = (((int64_t)w.b * a.S + ks + j) * a.Hkv + kvh) * D + d;
+                int64_t off = (((int64_t)w.b * a.S + slot_pos(g, ks + j)) * a.Hkv + kvh) * D + d;
                 kv = k[off];
                 vv = v[off];
             }
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
 #pragma unroll 8
             for (int d = 0; d < D; ++d) s = fma((double)Qs[rr][d], (double)Ks[lane][d], s);
             s *= scale;
-            const bool vis = lane < kl && (!a.causal || ks + lane <= qpos);
+            const bool vis = lane < kl && (!a.causal || ks + lane <= qpos + it.shift);
             if (!vis) s = -INFINITY;
             double mt = s;
 #pragma unroll
@@ -122,11 +122,12 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
         const int qpos = w.q0 + rr;
         if (qpos >= w.cend) continue;
         const double inv = l[i] > 0.0 ? 1.0 / l[i] : 0.0;
-        float *orow = out + (((int64_t)w.b * a.S + qpos) * a.Hq + w.h) * D;
+        const int qp = slot_pos(g, qpos);
+        float *orow = out + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) orow[lane + 32 * e] = (float)(o[i][e] * inv);
         if (lane == 0)
-            lse[((int64_t)w.b * a.Hq + w.h) * a.S + qpos] =
+            lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] =
                 l[i] > 0.0 ? (float)(m[i] + log(l[i])) : -INFINITY;
     }
 }

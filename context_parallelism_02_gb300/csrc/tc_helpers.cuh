@@ -101,6 +101,16 @@ __device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap *map, 
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load5(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                          int c0, int c1, int c2, int c3, int c4, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last()
 {
     uint64_t p;
@@ -187,17 +197,22 @@ inline EncodeFn get_encode()
     return fn;
 }
 
-// [B][S][H][D] bf16, box = 64 columns x box_rows rows of one (b, h), 128B swizzle.
+// [B][S][H][D] bf16 viewed as [B][S/R][R][H][D]; box = 64 columns x box_rows
+// rows of one (b, r, h), 128B swizzle.  R = N reads one rank of the striped
+// layout (consecutive rows N positions apart); R = 1 is the plain layout.
+// Coordinates (innermost first): column, head, r, row, batch.
 inline bool make_map(CUtensorMap *m, const void *ptr, int B, int64_t S, int H, int D,
-                     int box_rows = 128)
+                     int box_rows = 128, int R = 1)
 {
     EncodeFn enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
+    if (!enc || R < 1 || S % R) return false;
+    cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)R, (cuuint64_t)(S / R),
+                          (cuuint64_t)B};
+    cuuint64_t strides[4] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)R * H * D * 2,
+                             (cuuint64_t)S * H * D * 2};
+    cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

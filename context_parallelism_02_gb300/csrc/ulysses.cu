@@ -5,7 +5,7 @@
 // (all tokens, one group of H/P heads); the second turns it back.  With all N
 // ranks' buffers on one device the pair of collectives is a pure permutation:
 //   x[r][b][t][g*H/N + hh][:]  <->  y[g][b][pos(r, t)][hh][:]
-// where pos is the layout's shard map (contiguous or zigzag), so that each head
+// where pos is the layout's shard map (contiguous, zigzag or striped), so that each head
 // group sees the sequence in global order.
 //
 // The unit of copying is a run of H/N heads x D elements, contiguous on both
@@ -32,6 +32,11 @@ struct UlyArgs {
 // rank and local row of global position s
 __device__ __forceinline__ void locate(const Geom &g, int s, int &r, int &t)
 {
+    if (striped(g)) {
+        r = s % g.N;
+        t = s / g.N;
+        return;
+    }
     const int ch = s / g.clen;
     r = chunk_rank(g, ch);
     const int within = s - ch * g.clen;

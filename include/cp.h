@@ -22,7 +22,10 @@
  *   - causal: key j is visible to query i iff j <= i, in global positions.
  *   - layout: CP_LAYOUT_CONTIGUOUS splits S into N shards of S/N tokens;
  *     CP_LAYOUT_ZIGZAG splits S into 2N chunks and gives rank r chunks r and
- *     2N-1-r (local row order: chunk r first).
+ *     2N-1-r (local row order: chunk r first; S % 2N == 0);
+ *     CP_LAYOUT_STRIPED gives token p to rank p mod N ("Sequence Parallelism
+ *     in LLMs", "Causal Masking and Load Balancing", striped partitioning;
+ *     local row t of rank r is position r + N t).  S % N == 0 for all three.
  *   - Ring schedule: rank r at step k = 0..N-1 uses the KV shard of rank
  *     (r - k) mod N; N compute steps (step 0 is the local block).
  *   - Device pointers are caller-owned device memory (the library keeps no
@@ -55,6 +58,7 @@ extern "C" {
 /* sequence layouts */
 #define CP_LAYOUT_CONTIGUOUS 0
 #define CP_LAYOUT_ZIGZAG 1
+#define CP_LAYOUT_STRIPED 2
 
 /* element types of q, k, v, out (lse is always fp32) */
 #define CP_F32 0

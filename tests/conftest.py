@@ -19,8 +19,11 @@ def oracle():
     return _oracle
 
 
-# Tolerances (BASELINE workloads): bf16 inputs with fp32 accumulation,
-# fp32 inputs, and exact work for integer / byte paths.
+# Tolerances: bf16 inputs with fp32 accumulation, fp32 inputs, and exact work
+# for integer / byte paths.  The bf16 max bound is read relative to
+# max(1, |ref|): a bf16 output of magnitude 4..8 lies up to 2^-6 = 0.0156 away
+# from the exact value after rounding alone, so an absolute 1e-2 cannot hold
+# there even for an exact computation; below 1 the bound is absolute.
 BF16_MAX = 1e-2
 BF16_MEAN = 1e-3
 BF16_LSE = 1e-3

@@ -11,7 +11,7 @@ import pytest
 from context_parallelism_02_gb300 import _lib, api
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-CONT, ZIG = 0, 1
+CONT, ZIG, STR = 0, 1, 2
 
 
 def _declared_symbols():
@@ -35,7 +35,8 @@ def test_library_is_in_tree(cplib):
 
 
 @pytest.mark.parametrize("S,N,layout", [(8192, 8, CONT), (64, 4, ZIG), (1600, 4, ZIG),
-                                        (1000, 4, CONT), (48, 1, ZIG)])
+                                        (1000, 4, CONT), (48, 1, ZIG), (8192, 8, STR),
+                                        (1000, 4, STR), (99, 3, STR)])
 def test_shard_map_matches_oracle(cplib, oracle, S, N, layout):
     np.testing.assert_array_equal(api.cp_shard_map(S, N, layout), oracle.shard_pos(S, N, layout))
 
@@ -43,7 +44,9 @@ def test_shard_map_matches_oracle(cplib, oracle, S, N, layout):
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("S,N,layout", [(512, 4, CONT), (512, 4, ZIG), (8192, 8, ZIG),
                                         (8192, 8, CONT), (1600, 4, ZIG), (1000, 4, CONT),
-                                        (384, 1, ZIG), (96, 3, CONT)])
+                                        (384, 1, ZIG), (96, 3, CONT), (512, 4, STR),
+                                        (8192, 8, STR), (1000, 4, STR), (96, 3, STR),
+                                        (4096, 16, STR)])
 def test_schedule_pairs_match_oracle(cplib, oracle, S, N, layout, causal):
     """The kernel's tile schedule (tile skipping included) covers exactly the
     masked-in pairs of every (rank, step): bit-exact integer counts."""
@@ -69,6 +72,17 @@ def test_schedule_long_sequence_closed_forms(cplib):
     assert per_rank.max() - per_rank.min() <= 2
     full_pairs = S * (S + 1) // 2
     assert tz.sum() * 128 * 256 <= full_pairs * 1.01
+    # striped: every step of every rank has C(C+1)/2 - C [src > r] pairs, so
+    # every step (not only step 0) crosses the causal diagonal: each query row
+    # of each step wastes fewer than 256 masked columns (3 % of the work here)
+    ps, ts = api.cp_schedule_pairs(S, N, STR, True)
+    for r in range(N):
+        for k in range(N):
+            src = (r - k) % N
+            assert ps[r, k] == C * (C + 1) // 2 - (C if src > r else 0)
+    assert ps.sum() == full_pairs
+    assert np.all(ts == ts[0, 0])
+    assert ts.sum() * 128 * 256 <= full_pairs + N * N * C * 256
 
 
 def _call_fwd(**kw):
@@ -86,7 +100,10 @@ def test_argument_validation_without_gpu(cplib):
     assert _call_fwd(S=500, N=4) == _lib.CP_EINVAL            # zigzag needs S % 2N
     assert _call_fwd(S=510, N=4, layout=CONT) == _lib.CP_EINVAL
     assert _call_fwd(N=0) == _lib.CP_EINVAL
-    assert _call_fwd(layout=2) == _lib.CP_EINVAL
+    assert _call_fwd(layout=3) == _lib.CP_EINVAL
+    assert _call_fwd(layout=-1) == _lib.CP_EINVAL
+    assert _call_fwd(S=510, N=4, layout=STR) == _lib.CP_EINVAL     # striped needs S % N
+    assert _call_fwd(S=516, N=4, layout=STR) == _lib.CP_EINVAL     # null pointers (shape ok)
     assert _call_fwd(D=96) == _lib.CP_EUNSUPPORTED
     assert _call_fwd(dtype=7) == _lib.CP_EUNSUPPORTED
     assert _call_fwd() == _lib.CP_EINVAL                      # null pointers

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from context_parallelism_02_gb300 import api, inputs
-from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, ZIGZAG as ZIG, Workload
+from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, STRIPED as STR, ZIGZAG as ZIG, Workload
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +49,10 @@ SMALL = [
     ("n1_plain", 1, 2, 2, 640, 128, 1, CONT, True),
     ("chunk_below_tile", 1, 2, 2, 512, 64, 4, ZIG, True),
     ("n8_zig", 1, 2, 2, 4096, 128, 8, ZIG, True),
+    ("str_s1024_n4", 1, 2, 2, 1024, 128, 4, STR, True),
+    ("str_gqa_ragged_c400", 2, 4, 2, 1600, 128, 4, STR, True),
+    ("str_d64_n8", 1, 2, 1, 2048, 64, 8, STR, True),
+    ("str_noncausal", 1, 2, 2, 1536, 128, 2, STR, False),
 ]
 
 

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from context_parallelism_02_gb300 import api, inputs
-from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, ZIGZAG as ZIG, Workload
+from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, STRIPED as STR, ZIGZAG as ZIG, Workload
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +40,7 @@ def _check(name, got, ref):
 
 @pytest.mark.parametrize("qscale", [1.0, 8.0])
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("layout", [CONT, ZIG])
+@pytest.mark.parametrize("layout", [CONT, ZIG, STR])
 def test_tiny_fp32_bwd(cuda_dev, oracle, layout, causal, qscale):
     """The tiny workload (B=1, H=2, S=512, D=64, N=4) in fp32, every row."""
     w = inputs.TINY.with_(layout=layout, causal=causal, q_scale=qscale, with_grad=True)
@@ -58,6 +58,8 @@ F32_CASES = [
     ("d64_cont_noncausal", 1, 3, 1, 96, 64, 3, CONT, False),
     ("n1_plain", 1, 1, 1, 70, 128, 1, CONT, True),
     ("n8_zig_tiny_chunks", 1, 2, 2, 64, 64, 8, ZIG, True),   # chunks of 4 rows
+    ("str_gqa_ragged", 2, 4, 2, 200, 128, 4, STR, True),
+    ("str_n3_c23", 1, 2, 1, 69, 64, 3, STR, True),
 ]
 
 
@@ -75,12 +77,12 @@ def test_fp32_bwd_shapes(cuda_dev, oracle, case):
 
 def test_fp32_bwd_independent_of_n_and_layout(cuda_dev):
     """The gradient does not depend on the sharding ("What it does not change"):
-    fp32 results for N in {1, 2, 4, 8} and both layouts agree to 1e-5."""
+    fp32 results for N in {1, 2, 4, 8} and every layout agree to 1e-5."""
     base = Workload("f32inv", 1, 2, 2, 256, 64, 1, CONT, True, torch.float32, seed=62, with_grad=True)
     q, k, v, do = (t.to(cuda_dev) for t in inputs.make_qkv(base))
     res = []
     for N in (1, 2, 4, 8):
-        for layout in (CONT, ZIG):
+        for layout in (CONT, ZIG, STR):
             out, lse = api.ring_attn_fwd(q, k, v, N, layout, True)
             res.append(api.ring_attn_bwd(q, k, v, out, lse, do, N, layout, True))
     torch.cuda.synchronize()

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from context_parallelism_02_gb300 import CP_ETIMEOUT, api, inputs
-from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, ZIGZAG as ZIG
+from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, STRIPED as STR, ZIGZAG as ZIG
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +63,9 @@ ULY = [
     (8, 1, 256, 8, 128, torch.bfloat16, ZIG),
     (4, 1, 96, 4, 3, torch.bfloat16, CONT),      # 6-byte runs: narrow vectors
     (1, 1, 32, 3, 8, torch.float32, ZIG),
+    (4, 2, 128, 8, 16, torch.bfloat16, STR),
+    (8, 1, 256, 8, 128, torch.float32, STR),
+    (3, 1, 96, 6, 5, torch.bfloat16, STR),
 ]
 
 
