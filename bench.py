@@ -50,6 +50,7 @@ def workload(name):
     table = {
         "long128k_zigzag": inputs.LONG128K,
         "long128k_contiguous": inputs.LONG128K.with_(layout=inputs.CONTIGUOUS),
+        "long128k_striped": inputs.LONG128K.with_(layout=inputs.STRIPED),
         "s8192": inputs.S8K,
         "gqa32k": inputs.GQA32K,
     }
@@ -211,8 +212,8 @@ def time_events(fn, reps, stream):
 
 
 def extras(dev, stream, peaks):
-    """lse_merge and Ulysses relayout bandwidth, and per-rank work/time of the
-    long workload for contiguous vs zigzag."""
+    """lse_merge and Ulysses relayout bandwidth, per-rank work/time of the long
+    workload for contiguous vs zigzag vs striped, and the backward."""
     import torch
     from context_parallelism_02_gb300 import api, inputs
     hbm = peaks["hbm_gbs"]
@@ -248,7 +249,7 @@ def extras(dev, stream, peaks):
     res["bytes"] = nb
     out["ulysses_q_gqa32k"] = res
     del x, y, x2
-    # per-rank work and time, long workload, contiguous vs zigzag
+    # per-rank work and time, long workload, contiguous vs zigzag vs striped
     w = inputs.LONG128K
     g = torch.Generator(device=dev).manual_seed(w.seed)
     q = torch.randn(w.B, w.S, w.Hq, w.D, device=dev, generator=g).to(torch.bfloat16)
@@ -257,8 +258,11 @@ def extras(dev, stream, peaks):
     ob = torch.empty_like(q)
     lb_ = torch.empty(w.B, w.Hq, w.S, device=dev)
     per = {}
-    for layout in (inputs.CONTIGUOUS, inputs.ZIGZAG):
+    for layout in (inputs.CONTIGUOUS, inputs.ZIGZAG, inputs.STRIPED):
         pairs, tiles = api.cp_schedule_pairs(w.S, w.N, layout, True)
+        whole = lambda: api.ring_attn_fwd(q, k, v, w.N, layout, True, out=ob, lse=lb_, stream=stream)
+        whole()
+        ms_all = time_events(whole, 3, stream)
         times = []
         for r in range(w.N):
             fn = lambda: api.ring_attn_fwd(q, k, v, w.N, layout, True, out=ob, lse=lb_,
@@ -271,6 +275,9 @@ def extras(dev, stream, peaks):
             "work_max_over_mean": max(work) / (sum(work) / len(work)),
             "ms_per_rank": times,
             "time_max_over_mean": max(times) / (sum(times) / len(times)),
+            "ms_all_ranks": ms_all,
+            "TFLOP/s_all_ranks": fwd_flops(w) / ms_all / 1e9,
+            "executed_tiles_128x256": int(tiles.sum()) * w.B * w.Hq,
         }
     out["per_rank_long128k"] = per
     del q, k, v, ob, lb_

@@ -63,6 +63,7 @@ def _load():
             lib.or_ring_fwd.argtypes = [P, P, P, i32, i32, i32, i64, i32, i32, i32, i32,
                                         dbl, P, P]
             lib.or_lse_merge.argtypes = [P, P, P, P, i64, i32, P, P]
+            lib.or_lse_merge_n.argtypes = [P, P, i32, i64, i32, P, P]
             lib.or_ulysses_seq_to_head.argtypes = [P, P, i32, i64, i32, i32, i32, i32, i32]
             lib.or_ulysses_head_to_seq.argtypes = [P, P, i32, i64, i32, i32, i32, i32, i32]
             lib.or_attn_bwd.argtypes = [P, P, P, P, i32, i32, i32, i64, i32, i32, dbl,
@@ -168,6 +169,19 @@ def lse_merge(out_a, lse_a, out_b, lse_b):
     lse = np.zeros_like(lse_a)
     _check(_load().or_lse_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), rows, D,
                                 _ptr(out), _ptr(lse)), "lse_merge")
+    return out, lse
+
+
+def lse_merge_n(out_parts, lse_parts):
+    """Merge n normalised partials over disjoint key sets (fp64):
+    out_parts [n, rows, D], lse_parts [n, rows] -> (out [rows, D], lse [rows])."""
+    out_parts, lse_parts = _f64(out_parts), _f64(lse_parts)
+    n, rows = lse_parts.shape
+    D = out_parts.size // max(n * rows, 1)
+    out = np.zeros((rows, D))
+    lse = np.zeros(rows)
+    _check(_load().or_lse_merge_n(_ptr(out_parts), _ptr(lse_parts), n, rows, D, _ptr(out),
+                                  _ptr(lse)), "lse_merge_n")
     return out, lse
 
 

@@ -293,6 +293,40 @@ int or_lse_merge(const double *out_a, const double *lse_a, const double *out_b,
     return 0;
 }
 
+/* n-way merge of normalised partials over disjoint key sets, the same
+ * log-sum-exp combination taken over all n at once:
+ *   lse = ln sum_i e^{lse_i},  out = sum_i e^{lse_i - lse} out_i.
+ * out_parts [n][rows][D], lse_parts [n][rows]; partials with lse = -inf have
+ * weight 0; all empty gives (0, -inf). */
+int or_lse_merge_n(const double *out_parts, const double *lse_parts, int n, int64_t rows, int D,
+                   double *out, double *lse)
+{
+    if (n < 1 || rows < 0 || D < 1) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double m = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+            double li = lse_parts[(int64_t)i * rows + r];
+            if (li > m) m = li;
+        }
+        double *o = out + r * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (m == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double l = 0.0;
+        for (int i = 0; i < n; ++i) l += exp(lse_parts[(int64_t)i * rows + r] - m);
+        for (int i = 0; i < n; ++i) {
+            double w = exp(lse_parts[(int64_t)i * rows + r] - m) / l;
+            const double *x = out_parts + ((int64_t)i * rows + r) * D;
+            for (int d = 0; d < D; ++d) o[d] += w * x[d];
+        }
+        lse[r] = m + log(l);
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Ulysses relayout ("DeepSpeed Ulysses" diagram): rank r's sequence shard
  * [B, S/N, H, D] goes to head-group layout [B, S, H/N, D] on rank g, which

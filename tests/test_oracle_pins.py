@@ -305,6 +305,48 @@ def test_merge_split_keys(oracle):
     np.testing.assert_allclose(ya, yb, rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("cuts", [[0, 96], [0, 10, 96], [0, 5, 40, 41, 90, 96], [0, 1, 2, 3, 96]])
+def test_merge_n_split_keys(oracle, cuts):
+    """n disjoint key ranges computed separately and merged in one n-way step
+    equal attention over all keys ("Algorithmic Mechanics": the log-sum-exp
+    combination of partial results)."""
+    S, D = 96, 16
+    q, k, v = _rand((1, S, 2, D), 18, 2.0), _rand((1, S, 2, D), 19), _rand((1, S, 2, D), 20)
+    full, lfull = oracle.attn_fwd(q, k, v, False)
+    parts = [oracle.attn_fwd(q, k, v, False, klo=a, khi=b) for a, b in zip(cuts[:-1], cuts[1:])]
+    outs = np.stack([o.transpose(0, 2, 1, 3).reshape(-1, D) for o, _ in parts])
+    lses = np.stack([l.reshape(-1) for _, l in parts])
+    om, lm = oracle.lse_merge_n(outs, lses)
+    np.testing.assert_allclose(om, full.transpose(0, 2, 1, 3).reshape(-1, D), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lm, lfull.reshape(-1), rtol=0, atol=1e-13)
+    # independent of the order of the partials
+    perm = np.arange(len(parts))[::-1]
+    om2, lm2 = oracle.lse_merge_n(outs[perm], lses[perm])
+    np.testing.assert_allclose(om2, om, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lm2, lm, rtol=0, atol=1e-14)
+
+
+def test_merge_n_empty_partials(oracle):
+    """Partials with lse = -inf carry no weight; all empty gives (0, -inf);
+    n = 1 returns its input."""
+    rng = np.random.default_rng(1)
+    rows, D, n = 7, 4, 3
+    outs = rng.standard_normal((n, rows, D))
+    lses = rng.standard_normal((n, rows))
+    lses[1, :] = -np.inf
+    lses[:, 3] = -np.inf
+    om, lm = oracle.lse_merge_n(outs, lses)
+    keep = [0, 2]
+    o2, l2 = oracle.lse_merge_n(outs[keep], lses[keep])
+    np.testing.assert_array_equal(np.isneginf(lm), np.isneginf(l2))
+    np.testing.assert_allclose(om, o2, rtol=0, atol=1e-15)
+    assert np.all(om[3] == 0) and np.isneginf(lm[3])
+    o1, l1 = oracle.lse_merge_n(outs[:1], lses[:1])
+    fin = np.isfinite(lses[0])
+    np.testing.assert_allclose(o1[fin], outs[0][fin], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(l1[fin], lses[0][fin], rtol=0, atol=1e-15)
+
+
 def test_merge_neg_inf_identity(oracle):
     rng = np.random.default_rng(0)
     x = rng.standard_normal((5, 8))
