@@ -231,6 +231,19 @@ def extras(dev, stream, peaks):
     out["lse_merge"] = {"rows": rows, "D": D, "bytes": nbytes, "ms": ms,
                         "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm}
     del a, la, b, lb, o, lo
+    # lse_merge_n: n = 4 partials of the same rows (one pass, (n+1)(D+1)*4 B per row)
+    n_parts = 4
+    xs, ls = (t.to(dev) for t in inputs.make_merge_n_inputs(n_parts))
+    o = torch.empty(rows, D, device=dev)
+    lo = torch.empty(rows, device=dev)
+    nbytes = (n_parts + 1) * rows * (D + 1) * 4
+    f = lambda: api.lse_merge_n(xs, ls, out=o, lse=lo, stream=stream)
+    for _ in range(3):
+        f()
+    ms = time_events(f, 20, stream)
+    out["lse_merge_n4"] = {"rows": rows, "D": D, "n": n_parts, "bytes": nbytes, "ms": ms,
+                           "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm}
+    del xs, ls, o, lo
     # Ulysses relayout of the GQA workload's q (N=8, S=32768, H=32, D=128, bf16, zigzag)
     N, B, S, H, D = 8, 1, 32768, 32, 128
     x = torch.randn(N, B, S // N, H, D, device=dev).to(torch.bfloat16)

@@ -42,6 +42,7 @@ SIGNATURES = {
     "ring_attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I,
                                    _I, _I, _I, _F, _P]),
     "lse_merge": (_I, [_P, _P, _P, _P, _P, _P, _L, _I, _P]),
+    "lse_merge_n": (_I, [_P, _P, _I, _L, _I, _P, _P, _P]),
     "ulysses_seq_to_head": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),
     "ulysses_head_to_seq": (_I, [_P, _P, _I, _L, _I, _I, _I, _I, _I, _P]),
     "cp_get_error": (_I, [_P]),

@@ -162,6 +162,25 @@ def lse_merge(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
     return out, lse
 
 
+def lse_merge_n(out_parts, lse_parts, out=None, lse=None, stream=None):
+    """Merge n fp32 partials over disjoint key sets in one pass:
+    out_parts [n, rows, D], lse_parts [n, rows] -> (out [rows, D], lse [rows])."""
+    for name, t in (("out_parts", out_parts), ("lse_parts", lse_parts)):
+        _need_cuda_contig(name, t)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    n, rows = lse_parts.shape[0], lse_parts[0].numel()
+    D = out_parts.numel() // max(n * rows, 1)
+    if out is None:
+        out = torch.empty(rows, D, dtype=torch.float32, device=out_parts.device)
+    if lse is None:
+        lse = torch.empty(rows, dtype=torch.float32, device=out_parts.device)
+    rc = _lib.load().lse_merge_n(_ptr(out_parts), _ptr(lse_parts), n, rows, D, _ptr(out),
+                                 _ptr(lse), ctypes.c_void_p(_stream(stream)))
+    check(rc, "lse_merge_n")
+    return out, lse
+
+
 def ulysses_seq_to_head(x: torch.Tensor, N: int, layout: int, y=None, stream=None):
     """``[N, B, S/N, H, D]`` rank-major shards -> ``[N, B, S, H/N, D]`` head groups."""
     _need_cuda_contig("x", x)

@@ -254,6 +254,19 @@ int lse_merge(const float *out_a, const float *lse_a, const float *out_b, const 
                             static_cast<cudaStream_t>(stream));
 }
 
+int lse_merge_n(const float *out_parts, const float *lse_parts, int n, int64_t rows, int D,
+                float *out, float *lse, void *stream)
+{
+    if (n < 1 || rows < 0 || D < 4 || D % 4) return CP_EINVAL;
+    if (rows > INT64_MAX / D / n) return CP_EINVAL;
+    if (rows == 0) return CP_OK;
+    if (!out_parts || !lse_parts || !out || !lse) return CP_EINVAL;
+    if (!aligned16(out_parts) || !aligned16(out)) return CP_EINVAL;
+    if (((uintptr_t)lse_parts | (uintptr_t)lse) & 3u) return CP_EINVAL;
+    return launch_lse_merge_n(out_parts, lse_parts, n, rows, D, out, lse,
+                              static_cast<cudaStream_t>(stream));
+}
+
 static int ulysses_common(const void *src, void *dst, int B, int64_t S, int H, int D, int N,
                           int layout, int elem_bytes, int to_head, void *stream)
 {

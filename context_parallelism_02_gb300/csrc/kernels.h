@@ -22,6 +22,8 @@ int launch_fwd_f32(const float *q, const float *k, const float *v, float *out, f
                    FwdArgs a, cudaStream_t st);
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse,
                     FwdArgs a, cudaStream_t st);
+int launch_lse_merge_n(const float *out_parts, const float *lse_parts, int n, int64_t rows, int D,
+                       float *out, float *lse, cudaStream_t st);
 int launch_lse_merge(const float *out_a, const float *lse_a, const float *out_b,
                      const float *lse_b, float *out, float *lse, int64_t rows, int D,
                      cudaStream_t st);

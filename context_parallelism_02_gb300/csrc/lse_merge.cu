@@ -1,4 +1,4 @@
-// lse_merge.cu -- merge two normalised partial attention results.
+// lse_merge.cu -- merge two (or n) normalised partial attention results.
 //
 // "Sequence Parallelism in LLMs", "Algorithmic Mechanics" (online softmax
 // rescaling): with each partial carried as (out_x, lse_x) = (O, m + ln l),
@@ -84,7 +84,77 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float4 *xa,
     }
 }
 
+// n-way merge: lse = m + ln sum_i e^(lse_i - m), out = sum_i e^(lse_i - lse) out_i
+// with m = max_i lse_i.  One warp per row; every lane reads the n lse values
+// of the row (a broadcast load) and keeps its own column vectors, so out may
+// alias the first partial.  Partials are read four at a time to keep loads in
+// flight.
+__global__ void __launch_bounds__(256) lse_merge_n_kernel(const float4 *xs, const float *ls, int n,
+                                                          int64_t rows, int d4, float4 *xo, float *lo)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t pstride = rows * d4;   // float4s per partial
+    for (int64_t r = wid; r < rows; r += nw) {
+        float m = -INFINITY;
+        for (int i = 0; i < n; ++i) m = fmaxf(m, ls[(int64_t)i * rows + r]);
+        float l = 0.f;
+        if (m != -INFINITY)
+            for (int i = 0; i < n; ++i) l += expf(ls[(int64_t)i * rows + r] - m);
+        const float inv = m == -INFINITY ? 0.f : 1.f / l;
+        for (int c = lane; c < d4; c += 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 *x = xs + r * d4 + c;
+            int i = 0;
+            if (m != -INFINITY) {
+                for (; i + 4 <= n; i += 4) {
+                    float4 v[4];
+                    float w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        v[u] = x[(int64_t)(i + u) * pstride];
+                        w[u] = expf(ls[(int64_t)(i + u) * rows + r] - m) * inv;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        acc.x = fmaf(w[u], v[u].x, acc.x);
+                        acc.y = fmaf(w[u], v[u].y, acc.y);
+                        acc.z = fmaf(w[u], v[u].z, acc.z);
+                        acc.w = fmaf(w[u], v[u].w, acc.w);
+                    }
+                }
+                for (; i < n; ++i) {
+                    const float4 v = x[(int64_t)i * pstride];
+                    const float w = expf(ls[(int64_t)i * rows + r] - m) * inv;
+                    acc.x = fmaf(w, v.x, acc.x);
+                    acc.y = fmaf(w, v.y, acc.y);
+                    acc.z = fmaf(w, v.z, acc.z);
+                    acc.w = fmaf(w, v.w, acc.w);
+                }
+            }
+            xo[r * d4 + c] = acc;
+        }
+        // every lane has read the row's lse values before lane 0 overwrites one
+        __syncwarp();
+        if (lane == 0) lo[r] = m == -INFINITY ? -INFINITY : m + logf(l);
+    }
+}
+
 }  // namespace
+
+int launch_lse_merge_n(const float *out_parts, const float *lse_parts, int n, int64_t rows, int D,
+                       float *out, float *lse, cudaStream_t st)
+{
+    if (rows == 0) return CP_OK;
+    int64_t blocks = (rows + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    lse_merge_n_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+        reinterpret_cast<const float4 *>(out_parts), lse_parts, n, rows, D / 4,
+        reinterpret_cast<float4 *>(out), lse);
+    return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
+}
 
 int launch_lse_merge(const float *out_a, const float *lse_a, const float *out_b,
                      const float *lse_b, float *out, float *lse, int64_t rows, int D,

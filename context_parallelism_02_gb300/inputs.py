@@ -114,6 +114,20 @@ def make_merge_inputs(rows: int = MERGE_ROWS, D: int = MERGE_D, seed: int = MERG
     return out_a, lse_a, out_b, lse_b
 
 
+def make_merge_n_inputs(n: int, rows: int = MERGE_ROWS, D: int = MERGE_D, seed: int = MERGE_SEED,
+                        neg_inf_every: int = 0):
+    """n fp32 partial results (out_parts [n, rows, D], lse_parts [n, rows]) for
+    lse_merge_n, drawn like make_merge_inputs (lse ~ N(0, 4)).  With
+    ``neg_inf_every=k`` partial i has lse = -inf on every (k+i)-th row."""
+    g = torch.Generator().manual_seed(seed)
+    outs = draw((n, rows, D), g)
+    lses = draw((n, rows), g) * 2.0
+    if neg_inf_every:
+        for i in range(n):
+            lses[i, ::neg_inf_every + i] = float("-inf")
+    return outs, lses
+
+
 def make_layout_tensor(N: int, B: int, S: int, H: int, D: int, dtype: torch.dtype, seed: int):
     """A rank-major stack of N sequence shards, ``[N, B, S/N, H, D]``.
 

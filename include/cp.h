@@ -137,6 +137,23 @@ int lse_merge(const float *out_a, const float *lse_a, const float *out_b, const 
               float *out, float *lse, int64_t rows, int D, void *stream);
 
 /*
+ * lse_merge_n -- merge n normalised partial results over disjoint key sets in
+ * one pass: the log-sum-exp combination of lse_merge ("Algorithmic
+ * Mechanics") taken over all n at once,
+ *   lse = ln sum_i e^lse_i,  out = sum_i e^(lse_i - lse) out_i,
+ * e.g. the N per-step partials of one rank, or partials of a query row split
+ * across blocks.  Partials with lse = -inf drop out; all empty gives (0, -inf).
+ *   out_parts: device fp32 [n][rows][D]; lse_parts: device fp32 [n][rows];
+ *   out [rows][D], lse [rows]: device fp32.  out may alias one partial of
+ *   out_parts and lse one row set of lse_parts.
+ *   n >= 1, D % 4 == 0, rows >= 0 (rows == 0 is a no-op); HBM traffic is
+ *   (n + 1) (D + 1) 4 bytes per row.
+ * Errors: CP_EINVAL (null pointer, misalignment, n, D, size overflow), CP_ECUDA.
+ */
+int lse_merge_n(const float *out_parts, const float *lse_parts, int n, int64_t rows, int D,
+                float *out, float *lse, void *stream);
+
+/*
  * ulysses_seq_to_head / ulysses_head_to_seq -- the two all-to-all relayouts
  * of DeepSpeed-Ulysses done as one local permutation over all N ranks'
  * buffers ("Sequence Parallelism in LLMs", "DeepSpeed Ulysses": [Batch, S/P,

@@ -116,6 +116,10 @@ def test_argument_validation_without_gpu(cplib):
     assert L.ulysses_seq_to_head(None, None, 1, 64, 8, 8, 4, 0, 3, None) == _lib.CP_EINVAL
     assert L.lse_merge(None, None, None, None, None, None, 0, 128, None) == _lib.CP_OK
     assert L.lse_merge(None, None, None, None, None, None, 4, 6, None) == _lib.CP_EINVAL
+    assert L.lse_merge_n(None, None, 3, 0, 128, None, None, None) == _lib.CP_OK
+    assert L.lse_merge_n(None, None, 0, 4, 128, None, None, None) == _lib.CP_EINVAL
+    assert L.lse_merge_n(None, None, 3, 4, 6, None, None, None) == _lib.CP_EINVAL
+    assert L.lse_merge_n(None, None, 3, 4, 128, None, None, None) == _lib.CP_EINVAL
     buf = np.zeros(8, np.int32)
     assert L.cp_shard_map(12, 4, ZIG, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL
     assert L.cp_shard_map(1 << 40, 4, CONT, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL

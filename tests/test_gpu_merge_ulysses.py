@@ -56,6 +56,56 @@ def test_lse_merge_equals_attention_over_split_keys(cuda_dev, oracle):
     assert np.abs(lse.cpu().numpy() - lfull.reshape(-1)).max() <= 1e-5
 
 
+@pytest.mark.parametrize("n,rows,D,ninf", [(1, 1000, 128, 0), (2, 1000, 128, 3), (3, 4097, 64, 5),
+                                           (4, 1, 4, 0), (16, 2049, 128, 7), (5, 333, 12, 2)])
+def test_lse_merge_n_matches_oracle(cuda_dev, oracle, n, rows, D, ninf):
+    outs, lses = inputs.make_merge_n_inputs(n, rows, D, seed=33, neg_inf_every=ninf)
+    if ninf:
+        lses[:, 1] = float("-inf")        # a row where every partial is empty
+    out, lse = api.lse_merge_n(outs.to(cuda_dev), lses.to(cuda_dev))
+    torch.cuda.synchronize()
+    ref, lref = oracle.lse_merge_n(outs, lses)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    # fp32: n weighted terms and their sum, each rounded once (2^-24 relative),
+    # plus the weights' own rounding: (n + 2) ulps of the largest input
+    tol = (n + 2) * 2.0 ** -23 * max(1.0, float(outs.abs().max()))
+    assert np.abs(out - ref).max() <= tol
+    fin = np.isfinite(lref)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.abs(lse[fin] - lref[fin]).max(initial=0) <= 1e-6
+    if ninf:
+        assert np.all(out[1] == 0) and np.isneginf(lse[1])
+
+
+def test_lse_merge_n_equals_attention_and_in_place(cuda_dev, oracle):
+    """Attention over 4 disjoint key ranges merged in one n-way pass equals
+    attention over all keys; out and lse may alias the first partial."""
+    S, D = 120, 64
+    g = torch.Generator().manual_seed(6)
+    q, k, v = (torch.randn(1, S, 2, D, generator=g, dtype=torch.float64) for _ in range(3))
+    cuts = [0, 17, 60, 61, S]
+    parts = [oracle.attn_fwd(q, k, v, False, klo=a, khi=b) for a, b in zip(cuts[:-1], cuts[1:])]
+    outs = torch.from_numpy(np.stack([o.transpose(0, 2, 1, 3).reshape(-1, D) for o, _ in parts])).float()
+    lses = torch.from_numpy(np.stack([l.reshape(-1) for _, l in parts])).float()
+    go, gl = outs.to(cuda_dev), lses.to(cuda_dev)
+    out, lse = api.lse_merge_n(go, gl, out=go[0], lse=gl[0])
+    torch.cuda.synchronize()
+    full, lfull = oracle.attn_fwd(q, k, v, False)
+    assert np.abs(out.cpu().numpy() - full.transpose(0, 2, 1, 3).reshape(-1, D)).max() <= 1e-5
+    assert np.abs(lse.cpu().numpy() - lfull.reshape(-1)).max() <= 1e-5
+
+
+def test_lse_merge_n_full_size(cuda_dev, oracle):
+    """rows = 1x8x131072, D = 128, n = 4 partials: sampled rows against the oracle."""
+    outs, lses = inputs.make_merge_n_inputs(4)
+    out, lse = api.lse_merge_n(outs.to(cuda_dev), lses.to(cuda_dev))
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(4).integers(0, lses.shape[1], 4096)
+    ref, lref = oracle.lse_merge_n(outs[:, rows], lses[:, rows])
+    assert np.abs(out[rows].cpu().numpy() - ref).max() <= 6 * 2.0 ** -23 * float(outs.abs().max())
+    assert np.abs(lse[rows].cpu().numpy() - lref).max() <= 1e-6
+
+
 ULY = [
     # N, B, S, H, D, dtype, layout
     (2, 1, 64, 4, 8, torch.bfloat16, CONT),
