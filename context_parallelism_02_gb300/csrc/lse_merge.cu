@@ -141,14 +141,126 @@ __global__ void __launch_bounds__(256) lse_merge_n_kernel(const float4 *xs, cons
     }
 }
 
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int off = 16; off; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int off = 16; off; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// n <= 32: lane i holds partial i's weight (one exp per partial and row),
+// RPW rows per warp, the column vectors of up to 4 partials of every row in
+// flight before their weights are applied (4 rows for small n, where a row
+// alone moves too few bytes to cover the memory latency).
+template <int RPW>
+__global__ void __launch_bounds__(256) lse_merge_n32_kernel(const float4 *xs, const float *ls, int n,
+                                                            int64_t rows, int d4, float4 *xo, float *lo)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t pstride = rows * d4;   // float4s per partial
+    for (int64_t r0 = RPW * wid; r0 < rows; r0 += RPW * nw) {
+        float m[RPW], sum[RPW];
+        // the column loop runs the same number of times on every lane (the
+        // weight shuffles below need the whole warp); lanes past d4 only idle
+        for (int c0 = 0; c0 < d4; c0 += 32) {
+            const int c = c0 + lane;
+            const bool act = c < d4;
+            const float4 *x0 = xs + r0 * d4 + c;
+            // the first four partials' columns are requested before the
+            // weights, so that both memory latencies overlap
+            float4 v[RPW][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int j = 0; j < RPW; ++j) {
+                    v[j][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (act && u < n && r0 + j < rows) v[j][u] = x0[(int64_t)u * pstride + j * d4];
+                }
+            float w[RPW];
+#pragma unroll
+            for (int j = 0; j < RPW; ++j) {
+                const bool in = lane < n && r0 + j < rows;
+                const float a = in ? ls[(int64_t)lane * rows + r0 + j] : -INFINITY;
+                m[j] = warp_max(a);
+                const float e = m[j] == -INFINITY ? 0.f : expf(a - m[j]);
+                sum[j] = warp_sum(e);
+                w[j] = sum[j] > 0.f ? e / sum[j] : 0.f;
+            }
+            float4 acc[RPW];
+#pragma unroll
+            for (int j = 0; j < RPW; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < n; i += 4) {
+                if (i > 0) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int j = 0; j < RPW; ++j) {
+                            v[j][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (act && i + u < n && r0 + j < rows)
+                                v[j][u] = x0[(int64_t)(i + u) * pstride + j * d4];
+                        }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int j = 0; j < RPW; ++j) {
+                        const float q = __shfl_sync(0xffffffffu, w[j], (i + u) & 31);
+                        if (i + u < n) {
+                            acc[j].x = fmaf(q, v[j][u].x, acc[j].x);
+                            acc[j].y = fmaf(q, v[j][u].y, acc[j].y);
+                            acc[j].z = fmaf(q, v[j][u].z, acc[j].z);
+                            acc[j].w = fmaf(q, v[j][u].w, acc[j].w);
+                        }
+                    }
+            }
+            if (act) {
+#pragma unroll
+                for (int j = 0; j < RPW; ++j)
+                    if (r0 + j < rows) xo[(r0 + j) * d4 + c] = acc[j];
+            }
+        }
+        // every lane has read the rows' lse values before lane 0 overwrites them
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < RPW; ++j)
+                if (r0 + j < rows) lo[r0 + j] = m[j] == -INFINITY ? -INFINITY : m[j] + logf(sum[j]);
+        }
+    }
+}
+
 }  // namespace
 
 int launch_lse_merge_n(const float *out_parts, const float *lse_parts, int n, int64_t rows, int D,
                        float *out, float *lse, cudaStream_t st)
 {
     if (rows == 0) return CP_OK;
-    int64_t blocks = (rows + 7) / 8;
+    if (n == 2)   // the two-way kernel keeps more bytes in flight per warp
+        return launch_lse_merge(out_parts, lse_parts, out_parts + rows * D, lse_parts + rows, out, lse,
+                                rows, D, st);
     const int64_t cap = (int64_t)sm_count() * 8;
+    if (n <= 32) {
+        const int rpw = n <= 4 ? 4 : 2;
+        int64_t blocks = ((rows + rpw - 1) / rpw + 7) / 8;
+        if (blocks > cap) blocks = cap;
+        const float4 *xs = reinterpret_cast<const float4 *>(out_parts);
+        float4 *xo = reinterpret_cast<float4 *>(out);
+        if (rpw == 4)
+            lse_merge_n32_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(xs, lse_parts, n, rows, D / 4, xo, lse);
+        else
+            lse_merge_n32_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(xs, lse_parts, n, rows, D / 4, xo, lse);
+        return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
+    }
+    int64_t blocks = (rows + 7) / 8;
     if (blocks > cap) blocks = cap;
     lse_merge_n_kernel<<<(unsigned)blocks, 256, 0, st>>>(
         reinterpret_cast<const float4 *>(out_parts), lse_parts, n, rows, D / 4,

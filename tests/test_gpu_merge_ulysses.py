@@ -57,7 +57,8 @@ def test_lse_merge_equals_attention_over_split_keys(cuda_dev, oracle):
 
 
 @pytest.mark.parametrize("n,rows,D,ninf", [(1, 1000, 128, 0), (2, 1000, 128, 3), (3, 4097, 64, 5),
-                                           (4, 1, 4, 0), (16, 2049, 128, 7), (5, 333, 12, 2)])
+                                           (4, 1, 4, 0), (16, 2049, 128, 7), (5, 333, 12, 2),
+                                           (32, 64, 128, 9), (33, 257, 8, 4)])
 def test_lse_merge_n_matches_oracle(cuda_dev, oracle, n, rows, D, ninf):
     outs, lses = inputs.make_merge_n_inputs(n, rows, D, seed=33, neg_inf_every=ninf)
     if ninf:
