@@ -46,7 +46,7 @@ using namespace tc;
 
 constexpr int T = 128;             // tile rows (queries or keys)
 constexpr int NTHREADS = 384;
-constexpr int REGS_CTRL = 56;
+constexpr int REGS_CTRL = 88;
 constexpr int REGS_GRAD = 208;
 static_assert(128 * REGS_CTRL + 256 * REGS_GRAD <= NTHREADS * 168, "register split exceeds the launch budget");
 constexpr float LOG2E = 1.4426950408889634f;
@@ -448,10 +448,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(Q_SFREE));   // S(j+1) may be issued
+            // P = exp2(S sl2 - lse2); the per-element mask only where some row of
+            // the warp does not see the whole half tile
+            const bool full = __all_sync(0xffffffffu, lim >= 64);
             float p[64];
 #pragma unroll
-            for (int e = 0; e < 64; ++e)
-                p[e] = e < lim ? ex2(fmaf(__uint_as_float(sr[e]), sl2, -lse2)) : 0.f;
+            for (int e = 0; e < 64; e += 2) {
+                ffma2(p[e], p[e + 1], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]), sl2, -lse2);
+                p[e] = ex2(p[e]);
+                p[e + 1] = ex2(p[e + 1]);
+            }
+            if (!full) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) p[e] = e < lim ? p[e] : 0.f;
+            }
             if (!waitw(BAR(Q_PDONE), j & 1, wc)) {
                 ok = false;
                 break;
@@ -462,11 +472,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(Q_PFREE));   // dP(j+1) may be issued
+            // dS = P (dP - Delta)
             uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-                pk[e] = pack_bf16(p[2 * e] * (__uint_as_float(pr[2 * e]) - dlt),
-                                  p[2 * e + 1] * (__uint_as_float(pr[2 * e + 1]) - dlt));
+            for (int e = 0; e < 32; ++e) {
+                float t0, t1;
+                fadd2v(t0, t1, __uint_as_float(pr[2 * e]), __uint_as_float(pr[2 * e + 1]), -dlt, -dlt);
+                fmul2v(t0, t1, t0, t1, p[2 * e], p[2 * e + 1]);
+                pk[e] = pack_bf16(t0, t1);
+            }
             // dS(j) may be written once dQ(j-1) has read dS(j-1)
             if (j > 0 && !waitw(BAR(Q_DSFREE), (j - 1) & 1, wc)) {
                 ok = false;
@@ -635,14 +649,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int hs = s & 1;
                 const int qa = it.start() + 64 * hs, ql = it.len() - 64 * hs, h = it.head();
                 const int qr_rank = it.mrank(), qr_row = it.mrow() + 64 * hs;   // map coordinates
-                // per-row statistics of the half tile: lse (log2 units) and Delta
+                // per-row statistics of the half tile, negated: -lse (log2 units), -Delta
                 float *ls = stat + qr.st * 128, *dl = ls + 64;
                 for (int e = lane; e < 64; e += 32) {
                     float l2 = 0.f, dd = 0.f;
                     if (e < ql) {
                         const int64_t off = ((int64_t)w.b * a.Hq + h) * a.S + slot_pos(g, qa + e);
-                        l2 = lse[off] * LOG2E;
-                        dd = delta[off];
+                        l2 = -lse[off] * LOG2E;
+                        dd = -delta[off];
                     }
                     ls[e] = l2;
                     dl[e] = dd;
@@ -752,27 +766,57 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_ld2_x64(tb, sr, tb + 64u, pr);
             // visible query columns c: c < ql and (not causal or qa + c >= kpos)
             const int lo = a.causal ? kpos - sh - qa : 0;
-            const float4 *ls4 = reinterpret_cast<const float4 *>(stat + qr.st * 128);
-            const float4 *dl4 = ls4 + 16;
-            uint32_t pp[32], dd[32];
+            const float4 *ls4 = reinterpret_cast<const float4 *>(stat + qr.st * 128);   // -lse2
+            const float4 *dl4 = ls4 + 16;                                               // -Delta
+            // most tiles are visible to the whole warp: no per-element mask there
+            const bool full = __all_sync(0xffffffffu, lo <= 0 && ql >= 64);
+            // P^T (fp32, kept in place of S^T for dS^T) and its bf16 pairs, stored
+            // at once so that their registers are free for dS^T
+            {
+                uint32_t pp[32];
 #pragma unroll
-            for (int e4 = 0; e4 < 16; ++e4) {
-                const float4 l = ls4[e4], d = dl4[e4];
-                const float lv[4] = {l.x, l.y, l.z, l.w}, dv4[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-                for (int u = 0; u < 4; u += 2) {
-                    const int c0 = 4 * e4 + u, c1 = c0 + 1;
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[c0]), sl2, -lv[u]));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[c1]), sl2, -lv[u + 1]));
-                    const bool v0 = c0 >= lo && c0 < ql, v1 = c1 >= lo && c1 < ql;
-                    const float q0 = v0 ? p0 : 0.f, q1 = v1 ? p1 : 0.f;
-                    pp[c0 >> 1] = pack_bf16(q0, q1);
-                    dd[c0 >> 1] = pack_bf16(q0 * (__uint_as_float(pr[c0]) - dv4[u]),
-                                            q1 * (__uint_as_float(pr[c1]) - dv4[u + 1]));
+                for (int e4 = 0; e4 < 16; ++e4) {
+                    const float4 l = ls4[e4];
+                    const int c = 4 * e4;
+                    float p0, p1, p2, p3;
+                    ffma2v(p0, p1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, l.x, l.y);
+                    ffma2v(p2, p3, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]), sl2, sl2, l.z, l.w);
+                    p0 = ex2(p0);
+                    p1 = ex2(p1);
+                    p2 = ex2(p2);
+                    p3 = ex2(p3);
+                    if (!full) {
+                        p0 = (c >= lo && c < ql) ? p0 : 0.f;
+                        p1 = (c + 1 >= lo && c + 1 < ql) ? p1 : 0.f;
+                        p2 = (c + 2 >= lo && c + 2 < ql) ? p2 : 0.f;
+                        p3 = (c + 3 >= lo && c + 3 < ql) ? p3 : 0.f;
+                    }
+                    sr[c] = __float_as_uint(p0);
+                    sr[c + 1] = __float_as_uint(p1);
+                    sr[c + 2] = __float_as_uint(p2);
+                    sr[c + 3] = __float_as_uint(p3);
+                    pp[2 * e4] = pack_bf16(p0, p1);
+                    pp[2 * e4 + 1] = pack_bf16(p2, p3);
                 }
+                tmem_st_x32(tb, pp);
             }
-            tmem_st_x32(tb, pp);
-            tmem_st_x32(tb + 64u, dd);
+            {
+                // dS^T = P^T (dP^T - Delta)
+                uint32_t dd[32];
+#pragma unroll
+                for (int e4 = 0; e4 < 16; ++e4) {
+                    const float4 d = dl4[e4];
+                    const int c = 4 * e4;
+                    float t0, t1, t2, t3;
+                    fadd2v(t0, t1, __uint_as_float(pr[c]), __uint_as_float(pr[c + 1]), d.x, d.y);
+                    fadd2v(t2, t3, __uint_as_float(pr[c + 2]), __uint_as_float(pr[c + 3]), d.z, d.w);
+                    fmul2v(t0, t1, t0, t1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                    fmul2v(t2, t3, t2, t3, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                    dd[2 * e4] = pack_bf16(t0, t1);
+                    dd[2 * e4 + 1] = pack_bf16(t2, t3);
+                }
+                tmem_st_x32(tb + 64u, dd);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();

@@ -167,6 +167,38 @@ __device__ __forceinline__ void fadd2(float &s0, float &s1, float a0, float a1)
     asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(R));
 }
 
+// (d0, d1) = (a0*b0 + c0, a1*b1 + c1) on the paired fp32 pipe
+__device__ __forceinline__ void ffma2v(float &d0, float &d1, float a0, float a1, float b0, float b1,
+                                       float c0, float c1)
+{
+    uint64_t A, B, C, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c0), "f"(c1));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(R));
+}
+
+// (d0, d1) = (a0 + b0, a1 + b1) on the paired fp32 pipe
+__device__ __forceinline__ void fadd2v(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    uint64_t A, B, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(R));
+}
+
+// (d0, d1) = (a0 * b0, a1 * b1) on the paired fp32 pipe
+__device__ __forceinline__ void fmul2v(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    uint64_t A, B, R;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(R));
+}
+
 // two floats -> bf16x2 (round to nearest even), `lo` in the low half
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
