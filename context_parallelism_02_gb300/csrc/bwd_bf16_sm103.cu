@@ -532,8 +532,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // warpgroup s%2 turns them into P^T and dS^T (bf16 pairs, written over the
 // first half of the columns it read); then dV += P^T dO_s and dK += dS^T Q_s
 // (N=D, K=64).  With two buffers and one warpgroup per buffer, the MMAs of
-// step s+1 run while warpgroup s%2 works on step s, and the MMA issue order
-// dV/dK(s), S^T/dP^T(s+2) reuses buffer s%2 only after it has been read.
+// step s+1 run while warpgroup s%2 works on step s; S^T/dP^T(s+2) is issued
+// into buffer s%2 once dV/dK(s) has completed (a commit barrier, since the two
+// MMA groups come from different issuing threads).
 // Each gradient thread handles all 64 columns of its steps, so it moves them
 // with two 64-column tensor-memory loads and two 32-column stores.
 //
@@ -548,9 +549,10 @@ enum {
     K_QEMPTY = 1 + K_QST,         // K_QST half stages
     K_SDP = 1 + 2 * K_QST,        // 2 buffers: S^T, dP^T complete
     K_PDS = 3 + 2 * K_QST,        // 2 buffers: P^T, dS^T written (4 arrivals: one warpgroup)
-    K_FIN = 5 + 2 * K_QST,
-    K_DRAIN = 6 + 2 * K_QST,
-    K_NBAR = 7 + 2 * K_QST
+    K_BUF = 5 + 2 * K_QST,        // 2 buffers: dV/dK(s) complete, buffer s%2 may be rewritten
+    K_FIN = 7 + 2 * K_QST,
+    K_DRAIN = 8 + 2 * K_QST,      // one commit per issuing thread (2)
+    K_NBAR = 9 + 2 * K_QST
 };
 
 template <int D>
@@ -608,9 +610,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(K_SDP + i), 1);
             mbar_init(BAR(K_PDS + i), 4);
+            mbar_init(BAR(K_BUF + i), 1);
         }
         mbar_init(BAR(K_FIN), 1);
-        mbar_init(BAR(K_DRAIN), 1);
+        mbar_init(BAR(K_DRAIN), 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -684,49 +687,50 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int s = issued > K_QST ? issued - K_QST : 0; s < issued; ++s)
                     wait1(BAR(K_QFULL + s % K_QST), (s / K_QST) & 1, dc);
             }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
-            constexpr uint32_t idSP = idesc_bf16(128, 64, false);   // S^T, dP^T: N = 64 queries
-            constexpr uint32_t idKV = idesc_bf16(128, D, true);     // dV, dK: B MN-major
-            const uint64_t dKd = sdesc(sK, 16, 1024), dVd = sdesc(sV, 16, 1024);
-            const uint64_t dQ0 = sdesc(sQ, 16, 1024);                 // Q_s K-major (64-row boxes)
-            const uint64_t dQmn0 = sdesc(sQ, 8192, 1024);            // Q_s, dO_s MN-major
-            const uint32_t tDV = tmem + C::TM_DV, tDK = tmem + C::TM_DK;
-            // S^T(s), dP^T(s) into buffer s%2 from half stage `st`
-            auto issue_sdp = [&](int s, int st) {
-                const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
-                const uint64_t so = (uint64_t)(st * (C::STAGE >> 4));
-                ss_seq<0, D, 8192>(tb, dKd, dQ0 + so, idSP);
-                ss_seq<0, D, 8192>(tb + 64u, dVd, dQ0 + so + (uint64_t)(HB >> 4), idSP);
-                mma_commit(BAR(K_SDP + (s & 1)));
-            };
+        } else if ((warp == 1 || warp == 2) && lane == 0) {
+            // ------------------------------------------------------------ MMA issuers
+            // tcgen05.mma issue returns only once the MMAs are nearly done, so a
+            // single issuing thread leaves the tensor pipe idle while it waits on
+            // a barrier.  Two threads: warp 2 issues S^T/dP^T(s) into buffer s%2
+            // once dV/dK(s-2) has finished reading it; warp 1 issues dV/dK(s) once
+            // the gradient warpgroup has written P^T(s) and dS^T(s).
             bool ok = wait1(BAR(K_KVFULL), 0, wc);
-            Ring<K_QST> rs;      // stage of half step s
-            Ring<K_QST> rn;      // stage of half step s + 2
-            for (int i = 0; ok && i < 2 && i < ns; ++i, rn.next()) {
-                if (!wait1(BAR(K_QFULL + rn.st), rn.ph, wc)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                issue_sdp(i, rn.st);
-            }
-            for (int s = 0; ok && s < ns; ++s, rs.next(), rn.next()) {
-                if (!wait1(BAR(K_PDS + (s & 1)), (s >> 1) & 1, wc)) break;
-                tc_fence_after();
-                const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
-                const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
-                // dV += P^T dO_s, dK += dS^T Q_s (K = 64 queries: 4 MMAs each)
-                ts_mn_seq<0, 4, 0>(tDV, tb, dQmn0 + so + (uint64_t)(HB >> 4), idKV, s > 0 ? 1u : 0u);
-                ts_mn_seq<0, 4, 0>(tDK, tb + 64u, dQmn0 + so, idKV, s > 0 ? 1u : 0u);
-                mma_commit(BAR(K_QEMPTY + rs.st));
-                if (s + 2 < ns) {
-                    if (!wait1(BAR(K_QFULL + rn.st), rn.ph, wc)) break;
+            if (warp == 2) {
+                constexpr uint32_t idSP = idesc_bf16(128, 64, false);   // N = 64 queries
+                const uint64_t dKd = sdesc(sK, 16, 1024), dVd = sdesc(sV, 16, 1024);
+                const uint64_t dQ0 = sdesc(sQ, 16, 1024);               // Q_s K-major (64-row boxes)
+                Ring<K_QST> rs;
+                for (int s = 0; ok && s < ns; ++s, rs.next()) {
+                    if ((s >= 2 && !wait1(BAR(K_BUF + (s & 1)), ((s >> 1) - 1) & 1, wc)) ||
+                        !wait1(BAR(K_QFULL + rs.st), rs.ph, wc))
+                        break;
                     tc_fence_after();
-                    issue_sdp(s + 2, rn.st);
+                    const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
+                    const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
+                    ss_seq<0, D, 8192>(tb, dKd, dQ0 + so, idSP);
+                    ss_seq<0, D, 8192>(tb + 64u, dVd, dQ0 + so + (uint64_t)(HB >> 4), idSP);
+                    mma_commit(BAR(K_SDP + (s & 1)));
                 }
+            } else {
+                constexpr uint32_t idKV = idesc_bf16(128, D, true);     // dV, dK: B MN-major
+                const uint64_t dQmn0 = sdesc(sQ, 8192, 1024);          // Q_s, dO_s MN-major
+                const uint32_t tDV = tmem + C::TM_DV, tDK = tmem + C::TM_DK;
+                Ring<K_QST> rs;
+                for (int s = 0; ok && s < ns; ++s, rs.next()) {
+                    if (!wait1(BAR(K_PDS + (s & 1)), (s >> 1) & 1, wc)) break;
+                    tc_fence_after();
+                    const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
+                    const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
+                    // dV += P^T dO_s, dK += dS^T Q_s (K = 64 queries: 4 MMAs each)
+                    ts_mn_seq<0, 4, 0>(tDV, tb, dQmn0 + so + (uint64_t)(HB >> 4), idKV, s > 0 ? 1u : 0u);
+                    ts_mn_seq<0, 4, 0>(tDK, tb + 64u, dQmn0 + so, idKV, s > 0 ? 1u : 0u);
+                    // S^T/dP^T(s) completed before the gradient warps started, so the
+                    // stage is free once dV/dK(s) completes
+                    mma_commit(BAR(K_QEMPTY + rs.st));
+                    mma_commit(BAR(K_BUF + (s & 1)));
+                }
+                mma_commit(BAR(K_FIN));
             }
-            mma_commit(BAR(K_FIN));
             mma_commit(BAR(K_DRAIN));
             volatile int no_abort = 0;
             WaitCtl dc{a.err, &no_abort, a.limit_ns};
