@@ -526,7 +526,7 @@ def main():
 def kernel_sha():
     import hashlib
     h = hashlib.sha256()
-    for f in ("fwd_bf16_sm103.cu", "cp_common.cuh", "tmem_io.cuh"):
+    for f in ("fwd_bf16_sm103.cu", "cp_common.cuh", "tmem_io.cuh", "tc_helpers.cuh"):
         with open(os.path.join(ROOT, "context_parallelism_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -150,7 +150,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
-    const Unit w = decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, blockIdx.x);
+    // a launch over every rank numbers its units with each (batch, head)
+    // contiguous: the blocks in flight then stream the K/V of one or two heads,
+    // which stay in L2; a launch over a subset of ranks keeps heads fastest
+    const Unit w = (a.rank_lo == 0 && a.rank_hi == a.N)
+                       ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, blockIdx.x)
+                       : decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, blockIdx.x);
     const int kvh = w.h / (a.Hq / a.Hkv);
     const int n = KvIter<KT>::count(g, w.r, w.qmax);
 
