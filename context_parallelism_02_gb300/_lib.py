@@ -39,6 +39,9 @@ SIGNATURES = {
     "ring_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I,
                            _I, _F, _P, ctypes.c_size_t, _P]),
     "ring_attn_bwd_workspace": (ctypes.c_size_t, [_I, _I, _L]),
+    "usp_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _I, _F, _P,
+                          ctypes.c_size_t, _P]),
+    "usp_attn_fwd_workspace": (ctypes.c_size_t, [_I, _I, _L, _I, _I]),
     "ring_attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I,
                                    _I, _I, _I, _F, _P]),
     "lse_merge": (_I, [_P, _P, _P, _P, _P, _P, _L, _I, _P]),

@@ -88,6 +88,30 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, N: int, lay
     return out, lse
 
 
+def usp_attn_fwd(q, k, v, n_ulysses: int, n_ring: int, layout: int, causal: bool = True,
+                 scale: float | None = None, out=None, lse=None, workspace=None, stream=None):
+    """Attention on an n_ulysses x n_ring grid of virtual ranks (USP): heads split
+    by the Ulysses relayout, ring attention over n_ring ranks in each head group."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(name, t)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device)
+    ws_bytes = int(_lib.load().usp_attn_fwd_workspace(Hq, Hkv, S, D, _DT[q.dtype]))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    sc = -1.0 if scale is None else float(scale)
+    rc = _lib.load().usp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S,
+                                  D, n_ulysses, n_ring, int(causal), layout, _DT[q.dtype], sc,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  ctypes.c_void_p(_stream(stream)))
+    check(rc, "usp_attn_fwd")
+    return out, lse
+
+
 def ring_attn_bwd_workspace(B: int, Hq: int, S: int) -> int:
     return int(_lib.load().ring_attn_bwd_workspace(B, Hq, S))
 

@@ -267,6 +267,68 @@ int lse_merge_n(const float *out_parts, const float *lse_parts, int n, int64_t r
                               static_cast<cudaStream_t>(stream));
 }
 
+size_t usp_attn_fwd_workspace(int Hq, int Hkv, int64_t S, int D, int dtype)
+{
+    if (Hq < 1 || Hkv < 1 || S < 0 || D < 1 || (dtype != CP_F32 && dtype != CP_BF16)) return 0;
+    const size_t elem = dtype == CP_BF16 ? 2 : 4;
+    // one batch at a time: q and out (Hq heads), k and v (Hkv heads), head-group-major
+    const size_t b = (size_t)(2 * Hq + 2 * Hkv) * (size_t)S * (size_t)D * elem;
+    return (b + 255u) & ~(size_t)255u;
+}
+
+int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+                 int Hkv, int64_t S, int D, int n_ulysses, int n_ring, int causal, int layout,
+                 int dtype, float scale, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (n_ulysses < 1 || n_ring < 1 || B < 0 || Hq < 1 || Hkv < 1) return CP_EINVAL;
+    if (Hq % Hkv) return CP_EINVAL;
+    int rc = check_shard(S, n_ring, layout);
+    if (rc) return rc;
+    rc = check_shard(S, n_ulysses, CP_LAYOUT_CONTIGUOUS);
+    if (rc) return rc;
+    if (Hq % n_ulysses || Hkv % n_ulysses) return CP_EHEADS;   // P <= H_KV per Ulysses group
+    if (dtype != CP_F32 && dtype != CP_BF16) return CP_EUNSUPPORTED;
+    if (D != 64 && D != 128) return CP_EUNSUPPORTED;
+    if (B == 0 || S == 0) return CP_OK;
+    if (!q || !k || !v || !out || !lse || !workspace) return CP_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(workspace) ||
+        ((uintptr_t)lse & 3u))
+        return CP_EINVAL;
+    if (ws_bytes < usp_attn_fwd_workspace(Hq, Hkv, S, D, dtype)) return CP_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t elem = dtype == CP_BF16 ? 2 : 4;
+    const int hq = Hq / n_ulysses, hkv = Hkv / n_ulysses;
+    const int64_t rowq = S * Hq * D * elem, rowkv = S * Hkv * D * elem;   // bytes per batch
+    char *ws = static_cast<char *>(workspace);
+    char *yq = ws, *yk = yq + rowq, *yv = yk + rowkv, *yo = yv + rowkv;
+    for (int b = 0; b < B; ++b) {
+        // Ulysses all-to-all (seq -> head): batch b's [S][H][D] is the stack of
+        // n_ulysses sequence shards; each group u receives the whole sequence
+        // for heads [u H/n_ulysses, (u+1) H/n_ulysses)
+        const char *qb = static_cast<const char *>(q) + b * rowq;
+        const char *kb = static_cast<const char *>(k) + b * rowkv;
+        const char *vb = static_cast<const char *>(v) + b * rowkv;
+        if ((rc = launch_ulysses(qb, yq, 1, (int)S, Hq, D, n_ulysses, CP_LAYOUT_CONTIGUOUS, (int)elem, 1, st)) ||
+            (rc = launch_ulysses(kb, yk, 1, (int)S, Hkv, D, n_ulysses, CP_LAYOUT_CONTIGUOUS, (int)elem, 1, st)) ||
+            (rc = launch_ulysses(vb, yv, 1, (int)S, Hkv, D, n_ulysses, CP_LAYOUT_CONTIGUOUS, (int)elem, 1, st)))
+            return rc;
+        // ring attention within every head group over n_ring virtual ranks;
+        // the group's lse rows [b][u H/n_ulysses ...][S] are contiguous in lse
+        for (int u = 0; u < n_ulysses; ++u) {
+            rc = fwd_common(yq + u * S * hq * D * elem, yk + u * S * hkv * D * elem,
+                            yv + u * S * hkv * D * elem, yo + u * S * hq * D * elem,
+                            lse + ((int64_t)b * Hq + (int64_t)u * hq) * S, 1, hq, hkv, S, D, n_ring,
+                            causal, layout, dtype, scale, 0, n_ring, stream);
+            if (rc) return rc;
+        }
+        // the second all-to-all (head -> seq) puts out back in BSHD order
+        if ((rc = launch_ulysses(yo, static_cast<char *>(out) + b * rowq, 1, (int)S, Hq, D, n_ulysses,
+                                 CP_LAYOUT_CONTIGUOUS, (int)elem, 0, st)))
+            return rc;
+    }
+    return CP_OK;
+}
+
 static int ulysses_common(const void *src, void *dst, int B, int64_t S, int H, int D, int N,
                           int layout, int elem_bytes, int to_head, void *stream)
 {

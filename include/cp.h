@@ -173,6 +173,35 @@ int ulysses_head_to_seq(const void *y, void *x, int B, int64_t S, int H, int D, 
                         int layout, int elem_bytes, void *stream);
 
 /*
+ * usp_attn_fwd -- Unified Sequence Parallelism ("Sequence Parallelism in LLMs",
+ * "Unified Sequence Parallelism (USP / 2D SP)"): a 2-D grid of n_ulysses x
+ * n_ring virtual ranks.  The Ulysses dimension splits the heads with the
+ * all-to-all of "DeepSpeed Ulysses"; the ring dimension circulates K/V blocks
+ * as ring_attn_fwd does.  On one device, per batch: the seq->head relayout
+ * (ulysses_seq_to_head over n_ulysses contiguous shards) gives every Ulysses
+ * group u the whole sequence for heads [u H/n_ulysses, (u+1) H/n_ulysses);
+ * ring attention runs in each group over n_ring virtual ranks with the given
+ * layout; the head->seq relayout returns out to BSHD order.  The result is
+ * attention over all keys, as for ring_attn_fwd.
+ *   q, k, v, out, lse, causal, layout, dtype, scale: as ring_attn_fwd.
+ *   n_ulysses >= 1 must divide Hq and Hkv (the Ulysses head ceiling
+ *   P <= H_KV: CP_EHEADS otherwise) and S; n_ring >= 1 with the layout's
+ *   divisibility of S.
+ *   workspace: device, at least usp_attn_fwd_workspace(Hq, Hkv, S, D, dtype)
+ *   bytes, 16-byte aligned, caller-owned scratch (the head-group copies of one
+ *   batch); its contents on entry do not matter.
+ * Errors: as ring_attn_fwd, plus CP_EHEADS, and CP_EINVAL for a null or too
+ * small workspace.
+ */
+int usp_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+                 int Hkv, int64_t S, int D, int n_ulysses, int n_ring, int causal, int layout,
+                 int dtype, float scale, void *workspace, size_t ws_bytes, void *stream);
+
+/* usp_attn_fwd_workspace -- bytes of scratch usp_attn_fwd needs:
+ * (2 Hq + 2 Hkv) S D element bytes, rounded up to 256; 0 for bad sizes.  Host only. */
+size_t usp_attn_fwd_workspace(int Hq, int Hkv, int64_t S, int D, int dtype);
+
+/*
  * ring_attn_bwd -- gradients of L = sum(dout * out) for the ring forward
  * above.  The pages state that context parallelism leaves the gradients equal
  * to single-device training ("Sequence and Context Parallelism", "What it

@@ -116,6 +116,16 @@ def test_argument_validation_without_gpu(cplib):
     assert L.ulysses_seq_to_head(None, None, 1, 64, 8, 8, 4, 0, 3, None) == _lib.CP_EINVAL
     assert L.lse_merge(None, None, None, None, None, None, 0, 128, None) == _lib.CP_OK
     assert L.lse_merge(None, None, None, None, None, None, 4, 6, None) == _lib.CP_EINVAL
+    # USP: the Ulysses group size must divide the kv heads (P <= H_KV)
+    assert L.usp_attn_fwd(None, None, None, None, None, 1, 8, 2, 512, 64, 4, 2, 1, 1, 1, -1.0,
+                          None, 0, None) == _lib.CP_EHEADS
+    assert L.usp_attn_fwd(None, None, None, None, None, 1, 8, 4, 512, 64, 4, 2, 1, 1, 1, -1.0,
+                          None, 0, None) == _lib.CP_EINVAL          # null pointers / workspace
+    assert L.usp_attn_fwd(None, None, None, None, None, 1, 8, 4, 500, 64, 4, 2, 1, 0, 1, -1.0,
+                          None, 0, None) == _lib.CP_EINVAL          # S % n_ulysses
+    assert L.usp_attn_fwd(None, None, None, None, None, 0, 8, 4, 512, 64, 4, 2, 1, 1, 1, -1.0,
+                          None, 0, None) == _lib.CP_OK              # empty batch
+    assert L.usp_attn_fwd_workspace(8, 4, 512, 64, 1) == (2 * 8 + 2 * 4) * 512 * 64 * 2
     assert L.lse_merge_n(None, None, 3, 0, 128, None, None, None) == _lib.CP_OK
     assert L.lse_merge_n(None, None, 0, 4, 128, None, None, None) == _lib.CP_EINVAL
     assert L.lse_merge_n(None, None, 3, 4, 6, None, None, None) == _lib.CP_EINVAL
