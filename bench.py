@@ -283,7 +283,25 @@ def extras(dev, stream, peaks):
             fn()
             times.append(time_events(fn, 3, stream))
         work = (pairs.sum(1) * w.B * w.Hq).tolist()
+        # the same per-rank launches split-KV (ring_attn_fwd_split) at the count
+        # cp_fwd_split_count picks for each rank
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        nsp = [api.cp_fwd_split_count(w.B, w.Hq, w.S, w.D, w.N, layout, True, (r, r + 1), sms)
+               for r in range(w.N)]
+        ws = torch.empty(max(16, api.ring_attn_fwd_split_workspace(w.B, w.Hq, w.S, w.D, max(nsp))),
+                         dtype=torch.uint8, device=dev)
+        times_split = []
+        for r in range(w.N):
+            fn = lambda: api.ring_attn_fwd_split(q, k, v, w.N, layout, True, n_split=nsp[r], out=ob,
+                                                 lse=lb_, workspace=ws, stream=stream,
+                                                 rank_range=(r, r + 1))
+            fn()
+            times_split.append(time_events(fn, 3, stream))
+        del ws
         per[inputs.LAYOUT_NAMES[layout]] = {
+            "n_split_per_rank": nsp,
+            "ms_per_rank_split": times_split,
+            "split_max_rank_ms_vs_unsplit": [max(times_split), max(times)],
             "masked_in_pairs_per_rank": work,
             "work_max_over_mean": max(work) / (sum(work) / len(work)),
             "ms_per_rank": times,
@@ -294,6 +312,37 @@ def extras(dev, stream, peaks):
         }
     out["per_rank_long128k"] = per
     del q, k, v, ob, lb_
+    # split-KV forward where it pays: one head of the long workload, one rank
+    # per launch (64 query tiles of up to 512 KV tiles for 152 SMs), zigzag;
+    # each rank unsplit and at the count cp_fwd_split_count picks
+    w = inputs.LONG128K.with_(Hq=1, Hkv=1)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    q, k, v = (torch.randn(w.B, w.S, 1, w.D, device=dev, generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    ob = torch.empty_like(q)
+    lb_ = torch.empty(w.B, 1, w.S, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nsp = [api.cp_fwd_split_count(w.B, 1, w.S, w.D, w.N, w.layout, True, (r, r + 1), sms)
+           for r in range(w.N)]
+    ws = torch.empty(api.ring_attn_fwd_split_workspace(w.B, 1, w.S, w.D, max(nsp)),
+                     dtype=torch.uint8, device=dev)
+    t_un, t_sp = [], []
+    for r in range(w.N):
+        fu = lambda: api.ring_attn_fwd(q, k, v, w.N, w.layout, True, out=ob, lse=lb_, stream=stream,
+                                       rank_range=(r, r + 1))
+        fs = lambda: api.ring_attn_fwd_split(q, k, v, w.N, w.layout, True, n_split=nsp[r], out=ob,
+                                             lse=lb_, workspace=ws, stream=stream,
+                                             rank_range=(r, r + 1))
+        for f in (fu, fs):
+            f()
+        t_un.append(time_events(fu, 5, stream))
+        t_sp.append(time_events(fs, 5, stream))
+    out["split_kv_one_head_long128k"] = {
+        "workload": "B=1, H=1, S=131072, D=128, N=16, zigzag, causal; one launch per rank",
+        "n_split_per_rank": nsp, "ms_per_rank_unsplit": t_un, "ms_per_rank_split": t_sp,
+        "max_rank_ms_unsplit": max(t_un), "max_rank_ms_split": max(t_sp),
+        "speedup_max_rank": max(t_un) / max(t_sp)}
+    del q, k, v, ob, lb_, ws
     # backward: B=2, H=16, S=32768, D=128, N=8, zigzag, causal
     w = inputs.BWD32K
     g = torch.Generator(device=dev).manual_seed(w.seed)
@@ -490,7 +539,7 @@ def main():
                      "peak_source": f"{peak_src} bf16 dense ({peak_kind}; timed region "
                                     f"{args.steps * ms_local / 1e3:.2f} s)",
                      "frac_of_burst": achieved / peaks["bf16_tflops"],
-                     "kernel": "fwd_bf16_kernel<128>",
+                     "kernel": "fwd_bf16_kernel<128, false>",
                      "flops_per_launch": flops},
         "clocks": clocks,
         "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",

@@ -36,6 +36,10 @@ SIGNATURES = {
     "ring_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _P]),
     "ring_attn_fwd_rank": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _I,
                                 _I, _P]),
+    "ring_attn_fwd_split": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _I,
+                                 _I, _I, _P, ctypes.c_size_t, _P]),
+    "ring_attn_fwd_split_workspace": (ctypes.c_size_t, [_I, _I, _L, _I, _I]),
+    "cp_fwd_split_count": (_I, [_I, _I, _L, _I, _I, _I, _I, _I, _I, _I]),
     "ring_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I,
                            _I, _F, _P, ctypes.c_size_t, _P]),
     "ring_attn_bwd_workspace": (ctypes.c_size_t, [_I, _I, _L]),

@@ -88,6 +88,57 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, N: int, lay
     return out, lse
 
 
+def cp_fwd_split_count(B: int, Hq: int, S: int, D: int, N: int, layout: int, causal: bool = True,
+                       rank_range: tuple[int, int] | None = None, num_sms: int | None = None) -> int:
+    """Number of splits for :func:`ring_attn_fwd_split` (host-side dispatch
+    simulation); ``num_sms`` defaults to the current CUDA device's SM count."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    lo, hi = (0, N) if rank_range is None else rank_range
+    rc = _lib.load().cp_fwd_split_count(B, Hq, S, D, N, int(causal), layout, lo, hi, int(num_sms))
+    if rc < 1:
+        check(rc, "cp_fwd_split_count")
+    return rc
+
+
+def ring_attn_fwd_split_workspace(B: int, Hq: int, S: int, D: int, n_split: int) -> int:
+    return int(_lib.load().ring_attn_fwd_split_workspace(B, Hq, S, D, n_split))
+
+
+def ring_attn_fwd_split(q, k, v, N: int, layout: int, causal: bool = True, n_split: int | None = None,
+                        scale: float | None = None, out=None, lse=None, workspace=None, stream=None,
+                        rank_range: tuple[int, int] | None = None):
+    """Split-KV ring forward (bf16): every query tile's key walk cut into
+    ``n_split`` pieces on separate blocks, merged by log-sum-exp; returns
+    (out, lse).  ``n_split=None`` takes :func:`cp_fwd_split_count`;
+    ``workspace`` (at least ``ring_attn_fwd_split_workspace`` bytes) is
+    allocated with torch if None."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(name, t)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    lo, hi = (0, N) if rank_range is None else rank_range
+    if n_split is None:
+        n_split = cp_fwd_split_count(B, Hq, S, D, N, layout, causal, (lo, hi))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _need_cuda_contig("out", out)
+    _need_cuda_contig("lse", lse)
+    ws_bytes = ring_attn_fwd_split_workspace(B, Hq, S, D, n_split) if n_split >= 1 else 0
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    sc = -1.0 if scale is None else float(scale)
+    rc = _lib.load().ring_attn_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                         S, D, N, int(causal), layout, _DT.get(q.dtype, -1), sc, lo,
+                                         hi, n_split, _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         ctypes.c_void_p(_stream(stream)))
+    check(rc, "ring_attn_fwd_split")
+    return out, lse
+
+
 def usp_attn_fwd(q, k, v, n_ulysses: int, n_ring: int, layout: int, causal: bool = True,
                  scale: float | None = None, out=None, lse=None, workspace=None, stream=None):
     """Attention on an n_ulysses x n_ring grid of virtual ranks (USP): heads split

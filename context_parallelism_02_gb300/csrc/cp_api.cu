@@ -65,9 +65,12 @@ int64_t visible_pairs(int64_t qa, int64_t qb, int64_t ks, int64_t L)
     return sum;
 }
 
-int fwd_common(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
-               int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype, float scale,
-               int rank_lo, int rank_hi, void *stream)
+// Argument checks shared by the forward entry points (no CUDA call); fills a
+// except a.err.  Returns CP_OK, an error code, or 1 for an empty problem
+// (nothing to launch).
+int prepare_fwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype,
+                float scale, int rank_lo, int rank_hi, FwdArgs &a)
 {
     if (B < 0 || Hq < 1 || Hkv < 1 || (causal != 0 && causal != 1)) return CP_EINVAL;
     int rc = check_shard(S, N, layout);
@@ -76,11 +79,10 @@ int fwd_common(const void *q, const void *k, const void *v, void *out, float *ls
     if (rank_lo < 0 || rank_hi > N || rank_lo >= rank_hi) return CP_EINVAL;
     if (dtype != CP_F32 && dtype != CP_BF16) return CP_EUNSUPPORTED;
     if (D != 64 && D != 128) return CP_EUNSUPPORTED;
-    if (B == 0 || S == 0) return CP_OK;
+    if (B == 0 || S == 0) return 1;
     if (!q || !k || !v || !out || !lse) return CP_EINVAL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || ((uintptr_t)lse & 3u))
         return CP_EINVAL;
-    FwdArgs a;
     a.B = B;
     a.Hq = Hq;
     a.Hkv = Hkv;
@@ -93,14 +95,36 @@ int fwd_common(const void *q, const void *k, const void *v, void *out, float *ls
     a.rank_lo = rank_lo;
     a.rank_hi = rank_hi;
     a.upc = 0;
-    a.err = err_ptr();
+    a.err = nullptr;
     a.limit_ns = WAIT_LIMIT_NS;
+    return CP_OK;
+}
+
+int fwd_common(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Hq,
+               int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype, float scale,
+               int rank_lo, int rank_hi, void *stream)
+{
+    FwdArgs a;
+    const int rc = prepare_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, layout, dtype, scale,
+                               rank_lo, rank_hi, a);
+    if (rc) return rc == 1 ? CP_OK : rc;
+    a.err = err_ptr();
     if (!a.err) return CP_ECUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == CP_F32)
         return launch_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                               static_cast<const float *>(v), static_cast<float *>(out), lse, a, st);
     return launch_fwd_bf16(q, k, v, out, lse, a, st);
+}
+
+// Bytes of a split forward's partials: n (D + 1) fp32 per (batch, position,
+// head), rounded up to 256; 0 if that overflows.
+size_t split_workspace_bytes(int B, int Hq, int64_t S, int D, int n)
+{
+    const unsigned __int128 b = (unsigned __int128)n * (unsigned)B * (uint64_t)S * (unsigned)Hq *
+                                (unsigned)(D + 1) * 4u;
+    if (b > ((unsigned __int128)1 << 62)) return 0;
+    return (size_t)((b + 255) / 256 * 256);
 }
 
 }  // namespace
@@ -195,6 +219,54 @@ int ring_attn_fwd_rank(const void *q, const void *k, const void *v, void *out, f
 {
     return fwd_common(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, layout, dtype, scale,
                       rank_lo, rank_hi, stream);
+}
+
+size_t ring_attn_fwd_split_workspace(int B, int Hq, int64_t S, int D, int n_split)
+{
+    if (B < 0 || Hq < 0 || S < 0 || S > 0x7fffffffLL || (D != 64 && D != 128) || n_split < 1 ||
+        n_split > CP_MAX_SPLIT)
+        return 0;
+    return split_workspace_bytes(B, Hq, S, D, n_split);
+}
+
+int cp_fwd_split_count(int B, int Hq, int64_t S, int D, int N, int causal, int layout, int rank_lo,
+                       int rank_hi, int num_sms)
+{
+    if (B < 1 || Hq < 1 || (causal != 0 && causal != 1) || num_sms < 1) return CP_EINVAL;
+    int rc = check_shard(S, N, layout);
+    if (rc) return rc;
+    if (S == 0) return CP_EINVAL;
+    if (rank_lo < 0 || rank_hi > N || rank_lo >= rank_hi) return CP_EINVAL;
+    if (D != 64 && D != 128) return CP_EUNSUPPORTED;
+    return fwd_split_choose(B, Hq, (int)S, D, N, causal, layout, rank_lo, rank_hi, num_sms, 32);
+}
+
+int ring_attn_fwd_split(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                        int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype,
+                        float scale, int rank_lo, int rank_hi, int n_split, void *workspace,
+                        size_t ws_bytes, void *stream)
+{
+    if (n_split < 1 || n_split > CP_MAX_SPLIT) return CP_EINVAL;
+    FwdArgs a;
+    const int rc = prepare_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, layout, dtype, scale,
+                               rank_lo, rank_hi, a);
+    if (rc < 0) return rc;
+    if (dtype != CP_BF16) return CP_EUNSUPPORTED;
+    if (rc == 1) return CP_OK;
+    const size_t need = split_workspace_bytes(B, Hq, S, D, n_split);
+    if (n_split > 1 && (!workspace || !aligned16(workspace) || need == 0 || ws_bytes < need))
+        return CP_EINVAL;
+    a.err = err_ptr();
+    if (!a.err) return CP_ECUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_split == 1) return launch_fwd_bf16(q, k, v, out, lse, a, st);
+    SplitOut so;
+    so.n = n_split;
+    so.out = static_cast<float *>(workspace);
+    so.lse = so.out + (int64_t)n_split * B * S * Hq * D;
+    int r = launch_fwd_bf16_split(q, k, v, a, so, st);
+    if (r) return r;
+    return launch_fwd_split_combine(a, so, out, lse, st);
 }
 
 size_t ring_attn_bwd_workspace(int B, int Hq, int64_t S)

@@ -198,6 +198,16 @@ struct KvIter {
     {
         if (++t >= nt) advance_chunk();
     }
+    // Advance m tiles (whole chunks at a time where possible).
+    CP_HD void skip(int m)
+    {
+        while (m > 0 && valid()) {
+            const int take = nt - t < m ? nt - t : m;
+            t += take;
+            m -= take;
+            if (t >= nt) advance_chunk();
+        }
+    }
     // Total tiles of the walk (closed form per chunk).
     CP_HD static int count(const Geom &g, int r, int qmax)
     {

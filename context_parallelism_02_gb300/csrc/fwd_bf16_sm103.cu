@@ -127,11 +127,15 @@ __device__ __forceinline__ void issue_pv_seq(uint32_t tO, uint32_t tP, uint64_t 
 
 // --- the kernel ------------------------------------------------------------------
 
-template <int D>
+// SPLIT: the block runs split `sp` of its unit's walk (tiles [j0, j0 + n) of
+// the n_all tiles, cut into so.n nearly equal pieces) and writes the
+// normalised partial (out, lse) of those keys, in fp32, to so.out / so.lse at
+// the row index of the output row: [sp][B][S][Hq][D] and [sp][B][S][Hq].
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a, const float sl2,
-                    __nv_bfloat16 *__restrict__ out, float *__restrict__ lse)
+                    __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, const SplitOut so)
 {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -153,11 +157,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // a launch over every rank numbers its units with each (batch, head)
     // contiguous: the blocks in flight then stream the K/V of one or two heads,
     // which stay in L2; a launch over a subset of ranks keeps heads fastest
+    // split index slowest: the blocks in flight run the same split of
+    // consecutive units, which walk the same key tiles (as in an unsplit
+    // launch) and share them in L2; adjacent splits of one unit would walk
+    // disjoint key ranges and stream them from DRAM
+    const int nunits = SPLIT ? (int)(gridDim.x / (unsigned)so.n) : (int)gridDim.x;
+    const int sp = SPLIT ? (int)blockIdx.x / nunits : 0;
+    const int ublk = SPLIT ? (int)blockIdx.x - sp * nunits : (int)blockIdx.x;
     const Unit w = (a.rank_lo == 0 && a.rank_hi == a.N)
-                       ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, blockIdx.x)
-                       : decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, blockIdx.x);
+                       ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, ublk)
+                       : decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, ublk);
     const int kvh = w.h / (a.Hq / a.Hkv);
-    const int n = KvIter<KT>::count(g, w.r, w.qmax);
+    const int n_all = KvIter<KT>::count(g, w.r, w.qmax);
+    const int j0 = SPLIT ? (int)((int64_t)n_all * sp / so.n) : 0;
+    const int n = SPLIT ? (int)((int64_t)n_all * (sp + 1) / so.n) - j0 : n_all;
+    if (SPLIT && n == 0) {
+        // an empty split: the merge identity (out 0, lse -inf) for every row
+        const int rows = w.qmax - w.q0 + 1;
+        for (int i = threadIdx.x; i < rows * (D / 4); i += NTHREADS) {
+            const int rr = i / (D / 4), c4 = i - rr * (D / 4);
+            const int64_t orow = (((int64_t)sp * a.B + w.b) * a.S + slot_pos(g, w.q0 + rr)) * a.Hq + w.h;
+            reinterpret_cast<float4 *>(so.out + orow * D)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int rr = threadIdx.x; rr < rows; rr += NTHREADS)
+            so.lse[(((int64_t)sp * a.B + w.b) * a.S + slot_pos(g, w.q0 + rr)) * a.Hq + w.h] = -INFINITY;
+        return;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_Q), 1);
@@ -201,6 +226,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // K runs one tile ahead of V; the V loads reuse the K tile starts
             KvIter<KT> itk;
             itk.begin(g, w.r, w.qmax);
+            if (SPLIT) itk.skip(j0);
             int nk = 0, nv = 0;   // tiles whose K / V loads were issued
             int kr_cur = 0, kw_cur = 0, kr_next = 0, kw_next = 0;   // map coordinates (rank, row)
             bool ok = true;
@@ -322,6 +348,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
         KvIter<KT> it;
         it.begin(g, w.r, w.qmax);
+        if (SPLIT) it.skip(j0);
         for (int j = 0; j < n; ++j, it.next()) {
             if (!waitw(BAR(B_SFULL), j & 1, wc)) {
                 ok = false;
@@ -460,6 +487,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const bool valid = qpos < w.cend;
             const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const int qp = slot_pos(g, qpos);   // global position of the row
+            if constexpr (SPLIT) {
+                const int64_t prow = (((int64_t)sp * a.B + w.b) * a.S + qp) * a.Hq + w.h;
+                float *orow = so.out + prow * D + (D / 2) * half;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + 32u * c, o);
+                    if (valid) {
+                        float4 *dst = reinterpret_cast<float4 *>(orow + 32 * c);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                                  __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+                    }
+                }
+                if (ok && valid && half == 0)
+                    so.lse[prow] = l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
+            } else {
             __nv_bfloat16 *orow = out + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D + (D / 2) * half;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -481,6 +526,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (ok && valid && half == 0)
                 lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] =
                     l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
+            }
         }
         __syncwarp();
         tc_fence_before();
@@ -492,9 +538,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // --- host side -----------------------------------------------------------------
 
-template <int D>
+template <int D, bool SPLIT>
 int launch_d(const void *q, const void *k, const void *v, void *out, float *lse, FwdArgs a,
-             cudaStream_t st)
+             const SplitOut &so, cudaStream_t st)
 {
     CUtensorMap mq, mk, mv;
     const int R = a.layout == CP_LAYOUT_STRIPED ? a.N : 1;
@@ -505,7 +551,7 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CP_ECUDA;
     if (dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(fwd_bf16_kernel<D, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<D>::SMEM) != cudaSuccess)
             return CP_ECUDA;
         attr_done[dev] = true;
@@ -514,10 +560,11 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
     a.upc = (g.clen + QT - 1) / QT;
     const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
     if (units == 0) return CP_OK;
-    if (units > 0x7fffffffLL) return CP_EUNSUPPORTED;
+    const int64_t blocks = units * (SPLIT ? so.n : 1);
+    if (blocks > 0x7fffffffLL) return CP_EUNSUPPORTED;
     const float sl2 = a.scale * 1.4426950408889634f;
-    fwd_bf16_kernel<D><<<(unsigned)units, NTHREADS, Cfg<D>::SMEM, st>>>(
-        mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse);
+    fwd_bf16_kernel<D, SPLIT><<<(unsigned)blocks, NTHREADS, Cfg<D>::SMEM, st>>>(
+        mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse, so);
     return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
 }
 
@@ -526,8 +573,18 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse,
                     FwdArgs a, cudaStream_t st)
 {
-    if (a.D == 64) return launch_d<64>(q, k, v, out, lse, a, st);
-    if (a.D == 128) return launch_d<128>(q, k, v, out, lse, a, st);
+    const SplitOut none{1, nullptr, nullptr};
+    if (a.D == 64) return launch_d<64, false>(q, k, v, out, lse, a, none, st);
+    if (a.D == 128) return launch_d<128, false>(q, k, v, out, lse, a, none, st);
+    return CP_EUNSUPPORTED;
+}
+
+int launch_fwd_bf16_split(const void *q, const void *k, const void *v, FwdArgs a,
+                          const SplitOut &so, cudaStream_t st)
+{
+    if (so.n < 1 || !so.out || !so.lse) return CP_EINVAL;
+    if (a.D == 64) return launch_d<64, true>(q, k, v, nullptr, nullptr, a, so, st);
+    if (a.D == 128) return launch_d<128, true>(q, k, v, nullptr, nullptr, a, so, st);
     return CP_EUNSUPPORTED;
 }
 

@@ -18,10 +18,28 @@ struct FwdArgs {
     uint64_t limit_ns;    // bound of every device-side wait
 };
 
+// Partial results of a split forward (fp32, normalised): n splits of every
+// unit's key walk; out [n][B][S][Hq][D], lse [n][B][S][Hq].
+struct SplitOut {
+    int n;
+    float *out;
+    float *lse;
+};
+
 int launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse,
                    FwdArgs a, cudaStream_t st);
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse,
                     FwdArgs a, cudaStream_t st);
+int launch_fwd_bf16_split(const void *q, const void *k, const void *v, FwdArgs a,
+                          const SplitOut &so, cudaStream_t st);
+// Merge the so.n partials of the rows of ranks [a.rank_lo, a.rank_hi) into
+// out (bf16, [B][S][Hq][D]) and lse ([B][Hq][S]).
+int launch_fwd_split_combine(const FwdArgs &a, const SplitOut &so, void *out, float *lse,
+                             cudaStream_t st);
+// Number of splits for a split forward of these sizes on num_sms SMs (host;
+// 1 when splitting does not pay), at most max_split.
+int fwd_split_choose(int B, int Hq, int S, int D, int N, int causal, int layout, int rank_lo,
+                     int rank_hi, int num_sms, int max_split);
 int launch_lse_merge_n(const float *out_parts, const float *lse_parts, int n, int64_t rows, int D,
                        float *out, float *lse, cudaStream_t st);
 int launch_lse_merge(const float *out_a, const float *lse_a, const float *out_b,

@@ -122,6 +122,50 @@ int ring_attn_fwd_rank(const void *q, const void *k, const void *v, void *out, f
                        int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout,
                        int dtype, float scale, int rank_lo, int rank_hi, void *stream);
 
+/* Largest n_split ring_attn_fwd_split accepts. */
+#define CP_MAX_SPLIT 64
+
+/*
+ * ring_attn_fwd_split -- ring_attn_fwd_rank with every query tile's key walk
+ * (its N ring steps, in ring order) cut into n_split consecutive pieces, each
+ * run by its own thread block, and the pieces merged by log-sum-exp
+ * ("Algorithmic Mechanics", online softmax rescaling with lse = m + ln l:
+ * lse = ln sum_i e^lse_i, out = sum_i e^(lse_i - lse) out_i).  The pieces
+ * cover disjoint keys, so the result is the same attention, up to rounding.
+ * It spreads long query rows over more SMs when a launch has few or uneven
+ * query tiles (one rank's queries, few heads).
+ *   q, k, v, out, lse, B..scale, rank_lo, rank_hi: as ring_attn_fwd_rank;
+ *   dtype CP_BF16 only.
+ *   n_split: 1..CP_MAX_SPLIT; 1 runs ring_attn_fwd_rank (workspace unused).
+ *   workspace: device, at least ring_attn_fwd_split_workspace(B, Hq, S, D,
+ *   n_split) bytes, 16-byte aligned, caller-owned scratch (the fp32 partials);
+ *   its contents on entry do not matter.  Two launches on stream: the split
+ *   kernel, then the merge.
+ * Errors: as ring_attn_fwd_rank, plus CP_EINVAL (n_split out of range, null,
+ * misaligned or too small workspace) and CP_EUNSUPPORTED for CP_F32.
+ */
+int ring_attn_fwd_split(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                        int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout, int dtype,
+                        float scale, int rank_lo, int rank_hi, int n_split, void *workspace,
+                        size_t ws_bytes, void *stream);
+
+/* ring_attn_fwd_split_workspace -- bytes ring_attn_fwd_split needs:
+ * n_split B S Hq (D + 1) 4, rounded up to 256; 0 for bad sizes.  Host only. */
+size_t ring_attn_fwd_split_workspace(int B, int Hq, int64_t S, int D, int n_split);
+
+/*
+ * cp_fwd_split_count -- a number of splits for ring_attn_fwd_split on a
+ * device with num_sms SMs: the count (at most 32) that minimises the
+ * estimated time of a simulated dispatch of the blocks (launch order, one
+ * block per SM, cost = tiles walked + a fixed per-block overhead) plus the
+ * merge's HBM traffic; 1 when splitting does not pay.  Host only.
+ * Returns >= 1, or CP_EINVAL / CP_EUNSUPPORTED for arguments that
+ * ring_attn_fwd_split would reject (B, Hq, S, N, layout, rank range, D,
+ * num_sms < 1).
+ */
+int cp_fwd_split_count(int B, int Hq, int64_t S, int D, int N, int causal, int layout, int rank_lo,
+                       int rank_hi, int num_sms);
+
 /*
  * lse_merge -- merge two normalised partial attention results over disjoint
  * key sets ("Algorithmic Mechanics", online softmax rescaling, written with

@@ -130,8 +130,66 @@ def test_argument_validation_without_gpu(cplib):
     assert L.lse_merge_n(None, None, 0, 4, 128, None, None, None) == _lib.CP_EINVAL
     assert L.lse_merge_n(None, None, 3, 4, 6, None, None, None) == _lib.CP_EINVAL
     assert L.lse_merge_n(None, None, 3, 4, 128, None, None, None) == _lib.CP_EINVAL
+    # split-KV forward (bf16 only); fake non-null addresses are never touched
+    # because every check comes before the first CUDA call
+    fake = 1 << 20
+    split = lambda **kw: L.ring_attn_fwd_split(
+        *(kw.get(n, fake) for n in ("q", "k", "v", "out", "lse")), kw.get("B", 1), 8, 8,
+        kw.get("S", 8192), 128, kw.get("N", 8), 1, ZIG, kw.get("dtype", 1), -1.0, kw.get("lo", 0),
+        kw.get("hi", 8), kw.get("n_split", 4), kw.get("ws", fake), kw.get("ws_bytes", 1 << 40), None)
+    assert split(n_split=0) == _lib.CP_EINVAL
+    assert split(n_split=65) == _lib.CP_EINVAL
+    assert split(dtype=0) == _lib.CP_EUNSUPPORTED                     # CP_F32
+    assert split(q=None) == _lib.CP_EINVAL
+    assert split(ws=None) == _lib.CP_EINVAL
+    assert split(ws=fake + 8) == _lib.CP_EINVAL                       # misaligned workspace
+    need = L.ring_attn_fwd_split_workspace(1, 8, 8192, 128, 4)
+    assert split(ws_bytes=need - 1) == _lib.CP_EINVAL
+    assert split(lo=3, hi=3) == _lib.CP_EINVAL
+    assert split(S=8200) == _lib.CP_EINVAL                            # zigzag: S % 2N
+    assert split(B=0) == _lib.CP_OK                                   # empty batch
     buf = np.zeros(8, np.int32)
     assert L.cp_shard_map(12, 4, ZIG, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL
     assert L.cp_shard_map(1 << 40, 4, CONT, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL
     for code in (0, -1, -2, -3, -4, -5, -99):
         assert isinstance(_lib.strerror(code), str) and _lib.strerror(code)
+
+
+def test_split_workspace_size(cplib):
+    L = _lib.load()
+    for B, Hq, S, D, n in ((1, 8, 131072, 128, 4), (2, 3, 70, 64, 7), (1, 1, 1, 64, 1)):
+        raw = n * B * S * Hq * (D + 1) * 4
+        assert L.ring_attn_fwd_split_workspace(B, Hq, S, D, n) == (raw + 255) // 256 * 256
+    assert L.ring_attn_fwd_split_workspace(1, 8, 4096, 96, 2) == 0
+    assert L.ring_attn_fwd_split_workspace(1, 8, 4096, 128, 0) == 0
+    assert L.ring_attn_fwd_split_workspace(1, 8, 4096, 128, 65) == 0
+    assert L.ring_attn_fwd_split_workspace(1, 8, 1 << 31, 128, 4) == 0
+
+
+def test_split_count_choice(cplib):
+    """The split count from the dispatch simulation: 1 when the launch has many
+    waves of units, more than 1 when a few long query tiles would hold the
+    last wave, never above 32, and errors for what the split call rejects."""
+    L = _lib.load()
+    count = lambda B, Hq, S, N, layout, lo, hi, causal=1, D=128, sms=152: L.cp_fwd_split_count(
+        B, Hq, S, D, N, causal, layout, lo, hi, sms)
+    assert count(1, 8, 131072, 16, ZIG, 0, 16) == 1          # 8192 units: 54 waves
+    assert count(2, 16, 32768, 8, ZIG, 0, 8) == 1
+    assert count(1, 32, 32768, 8, ZIG, 0, 8) == 1
+    # one rank of the 128k ring (512 units): the counts that timed fastest
+    assert count(1, 8, 131072, 16, ZIG, 15, 16) == 2
+    assert count(1, 8, 131072, 16, CONT, 15, 16) == 2
+    assert count(1, 8, 131072, 16, CONT, 0, 1) == 1
+    # one head of it: 64 units of up to 512 tiles for 152 SMs
+    assert count(1, 1, 131072, 16, ZIG, 0, 1) >= 4
+    # 128 equal units (non-causal, 256 tiles each) on 300 SMs: 2 splits fill
+    # one wave exactly, 3 would need a second wave (the choice is not monotonic
+    # in the SM count)
+    assert count(1, 1, 65536, 4, ZIG, 0, 1, causal=0, sms=300) == 2
+    assert count(1, 1, 65536, 4, ZIG, 0, 1, causal=0, sms=152) == 1
+    for args in ((1, 1, 4096, 2, CONT, 0, 1), (3, 5, 1000, 4, STR, 1, 3), (1, 2, 640, 5, ZIG, 0, 5)):
+        assert 1 <= count(*args) <= 32
+    assert count(1, 8, 8192, 8, ZIG, 0, 8, sms=0) == _lib.CP_EINVAL
+    assert count(1, 8, 8200, 8, ZIG, 0, 8) == _lib.CP_EINVAL
+    assert count(1, 8, 8192, 8, ZIG, 4, 4) == _lib.CP_EINVAL
+    assert count(1, 8, 8192, 8, ZIG, 0, 8, D=96) == _lib.CP_EUNSUPPORTED
