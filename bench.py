@@ -526,6 +526,22 @@ def main():
     e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e2e_steps, world, dev)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    # the host link alone (one upload, one read-back, nothing else running): the
+    # pipelined steps are copy-bound when (h2d + d2h) / link rate exceeds the
+    # forward's time
+    link = {}
+    for name, st_, fn in (("h2d", up, lambda: upload(0)),
+                          ("d2h", down, lambda: [h_.copy_(d_, non_blocking=True)
+                                                 for h_, d_ in zip(outs_h[0], outs[0])])):
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st_):
+            a0.record(st_)
+            fn()
+            a1.record(st_)
+        torch.cuda.synchronize()
+        link[name] = (h2d if name == "h2d" else d2h) / a0.elapsed_time(a1) / 1e6
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -545,6 +561,7 @@ def main():
         "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": e2e_steps,
+                "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"],
                 "note": "pinned host buffers; uploads and read-backs of neighbouring steps "
                         "overlap the forward on two copy streams"},
         "gpu_launches": args.steps,

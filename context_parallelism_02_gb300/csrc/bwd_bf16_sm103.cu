@@ -145,49 +145,51 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__r
 // ----------------------------------------------------------------------------- dQ
 //
 // Query-stationary.  Tensor memory (columns): S [0,128), dP [128,256), the dQ
-// accumulator [256, 256+D), dS in bf16 pairs [256+D, 320+D), and Q in bf16
-// pairs [320+D, 320+3D/2).  Q is the same for every KV tile of the block, so
-// the gradient warps write it into tensor memory once and S = Q K^T takes its
-// A operand from there; shared memory holds dO, four K stages and two V stages.
+// accumulator [256, 256+D), dS in bf16 pairs [256+D, 320+D).  Shared memory
+// holds the block's Q and dO tiles, three K stages and two V stages: both
+// operands of S = Q K^T and dP = dO V^T come from shared memory, and only
+// dQ += dS K reads its A operand from tensor memory, which the gradient warps
+// load from and store to on every tile.
 //
 // S(j) and dP(j) have their own barriers both ways, so S(j+1) is issued as
 // soon as the gradient warps have read S(j) and runs while they read dP(j)
 // and compute; dQ(j) comes last.  K_j is read by S(j) and by dQ(j); with the
-// MMA order S(j+1), dP(j+1), dQ(j) the load of K(j+4) into the stage of K(j)
-// has three tile groups of MMAs to land.
+// MMA order S(j+1), dP(j+1), dQ(j) the load of K(j+3) into the stage of K(j)
+// has two tile groups of MMAs to land.
 
-constexpr int Q_KST = 4;
+constexpr int Q_KST = 3;
 enum {
-    Q_QTM = 0,       // Q written into tensor memory: one arrival per gradient warp (8)
-    Q_DOFULL = 1,    // dO tile landed
-    Q_KFULL = 2,     // Q_KST stages
-    Q_KEMPTY = 6,    // Q_KST stages; commits after S(j) and after dQ(j)
-    Q_VFULL = 10,    // 2 stages
-    Q_VEMPTY = 12,   // 2 stages
-    Q_SDONE = 14,    // S(j) complete
-    Q_PDONE = 15,    // dP(j) complete
-    Q_SFREE = 16,    // S(j) read by the gradient warps (8 arrivals)
-    Q_PFREE = 17,    // dP(j) read (8 arrivals)
-    Q_DS = 18,       // dS(j) written (8 arrivals)
-    Q_DSFREE = 19,   // dQ(j) complete: the dS columns may be rewritten
-    Q_FIN = 20,
-    Q_DRAIN = 21,    // one commit per issuer (2)
-    Q_NBAR = 22
+    Q_QTM = 0,                   // Q tile landed
+    Q_DOFULL = 1,                // dO tile landed
+    Q_KFULL = 2,                 // Q_KST stages
+    Q_KEMPTY = 2 + Q_KST,        // Q_KST stages; commits after S(j) and after dQ(j)
+    Q_VFULL = 2 + 2 * Q_KST,     // 2 stages
+    Q_VEMPTY = 4 + 2 * Q_KST,    // 2 stages
+    Q_SDONE = 6 + 2 * Q_KST,     // S(j) complete
+    Q_PDONE = 7 + 2 * Q_KST,     // dP(j) complete
+    Q_SFREE = 8 + 2 * Q_KST,     // S(j) read by the gradient warps (8 arrivals)
+    Q_PFREE = 9 + 2 * Q_KST,     // dP(j) read (8 arrivals)
+    Q_DS = 10 + 2 * Q_KST,       // dS(j) written (8 arrivals)
+    Q_DSFREE = 11 + 2 * Q_KST,   // dQ(j) complete: the dS columns may be rewritten
+    Q_FIN = 12 + 2 * Q_KST,
+    Q_DRAIN = 13 + 2 * Q_KST,    // one commit per issuer (2)
+    Q_NBAR = 14 + 2 * Q_KST
 };
 
 template <int D>
 struct DqCfg {
     static constexpr int TB = Tile<D>::BYTES;
     static constexpr int OFF_DO = 0;
-    static constexpr int OFF_K = TB;                    // Q_KST stages
-    static constexpr int OFF_V = (1 + Q_KST) * TB;      // 2 stages
-    static constexpr int OFF_BAR = (3 + Q_KST) * TB;
+    static constexpr int OFF_Q = TB;
+    static constexpr int OFF_K = 2 * TB;                // Q_KST stages
+    static constexpr int OFF_V = (2 + Q_KST) * TB;      // 2 stages
+    static constexpr int OFF_BAR = (4 + Q_KST) * TB;
     static constexpr int OFF_MISC = OFF_BAR + 8 * Q_NBAR;
     static constexpr int NEED = OFF_MISC + 16;
     static constexpr int SMEM = NEED > 120 * 1024 ? NEED : 120 * 1024;
     static_assert(SMEM <= 232448, "dQ kernel shared memory");
-    static constexpr uint32_t TM_S = 0, TM_P = 128, TM_DQ = 256, TM_DS = 256 + D, TM_Q = 320 + D;
-    static_assert(TM_Q + D / 2 <= 512, "dQ kernel tensor memory");
+    static constexpr uint32_t TM_S = 0, TM_P = 128, TM_DQ = 256, TM_DS = 256 + D;
+    static_assert(TM_DS + 64 <= 512, "dQ kernel tensor memory");
 };
 
 // stage index and phase parity of a ring of NS buffers, advanced once per use
@@ -214,9 +216,9 @@ struct BwdArgs {
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmDO, const BwdArgs a,
-                  const __nv_bfloat16 *__restrict__ q, const float *__restrict__ lse,
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdArgs a, const float *__restrict__ lse,
                   const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dq)
 {
     using C = DqCfg<D>;
@@ -227,8 +229,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_TIMEOUT);
         return;
     }
-    const uint32_t sDO = base + C::OFF_DO, sK = base + C::OFF_K, sV = base + C::OFF_V,
-                   bar0 = base + C::OFF_BAR;
+    const uint32_t sDO = base + C::OFF_DO, sQ = base + C::OFF_Q, sK = base + C::OFF_K,
+                   sV = base + C::OFF_V, bar0 = base + C::OFF_BAR;
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + C::OFF_MISC + 4);
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int n = KvIter<T>::count(g, w.r, w.qmax);
 
     if (threadIdx.x == 0) {
-        mbar_init(BAR(Q_QTM), 8);
+        mbar_init(BAR(Q_QTM), 1);
         mbar_init(BAR(Q_DOFULL), 1);
         for (int i = 0; i < Q_KST; ++i) {
             mbar_init(BAR(Q_KFULL + i), 1);
@@ -300,6 +302,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         } else if (warp == 3 && lane == 0) {
             // ------------------------------------------------------------ dO and V producer
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+            mbar_arrive_expect_tx(BAR(Q_QTM), TB);
+            for (int bx = 0; bx < D / 64; ++bx)
+                tma_load5(sQ + bx * 16384, &tmQ, BAR(Q_QTM), bx * 64, w.h, slot_mrank(g, w.q0),
+                          slot_mrow(g, w.q0), w.b, pol_q);
             mbar_arrive_expect_tx(BAR(Q_DOFULL), TB);
             for (int bx = 0; bx < D / 64; ++bx)
                 tma_load5(sDO + bx * 16384, &tmDO, BAR(Q_DOFULL), bx * 64, w.h, slot_mrank(g, w.q0),
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (*abort_flag) {
                 volatile int no_abort = 0;
                 WaitCtl dc{a.err, &no_abort, a.limit_ns};
+                wait1(BAR(Q_QTM), 0, dc);
                 wait1(BAR(Q_DOFULL), 0, dc);
                 for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) wait1(BAR(Q_VFULL + (j & 1)), (j >> 1) & 1, dc);
             }
@@ -329,10 +336,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t idSP = idesc_bf16(128, T, false);     // K-major A and B
             constexpr uint32_t idDQ = idesc_bf16(128, D, true);      // B = K MN-major
             const uint32_t tS = tmem + C::TM_S, tP = tmem + C::TM_P, tDQ = tmem + C::TM_DQ,
-                           tDS = tmem + C::TM_DS, tQ = tmem + C::TM_Q;
+                           tDS = tmem + C::TM_DS;
             bool ok = true;
             if (warp == 1) {
-                const uint64_t dDOd = sdesc(sDO, 16, 1024);
+                const uint64_t dDOd = sdesc(sDO, 16, 1024), dQd = sdesc(sQ, 16, 1024);
                 const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, 16, 1024);
                 ok = wait1(BAR(Q_QTM), 0, wc) && wait1(BAR(Q_DOFULL), 0, wc);
                 Ring<Q_KST> kr;
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         !wait1(BAR(Q_KFULL + kr.st), kr.ph, wc))
                         break;
                     tc_fence_after();
-                    tsk_seq<0, D>(tS, tQ, dK0 + (uint64_t)(kr.st * (TB >> 4)), idSP);
+                    ss_seq<0, D, 16384>(tS, dQd, dK0 + (uint64_t)(kr.st * (TB >> 4)), idSP);
                     mma_commit(BAR(Q_SDONE));
                     mma_commit(BAR(Q_KEMPTY + kr.st));
                     if ((j > 0 && !wait1(BAR(Q_PFREE), (j - 1) & 1, wc)) ||
@@ -394,33 +401,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int qpos = w.q0 + row;                  // slot
         const int qp = slot_pos(g, qpos);             // global position
         const bool valid = qpos < w.cend;
-        {
-            // this half's D/2 elements of the Q row, as D/4 bf16 pairs (rows past the
-            // unit's chunk are zero; their results are never stored)
-            uint32_t qv[D / 4];
-            if (valid) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    q + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D + (D / 2) * half);
-#pragma unroll
-                for (int i = 0; i < D / 16; ++i) {
-                    const uint4 x = src[i];
-                    qv[4 * i] = x.x;
-                    qv[4 * i + 1] = x.y;
-                    qv[4 * i + 2] = x.z;
-                    qv[4 * i + 3] = x.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < D / 4; ++i) qv[i] = 0u;
-            }
-            const uint32_t tQ = tmem + lane_off + C::TM_Q + (D / 4) * half;
-            if constexpr (D == 128) tmem_st_x32(tQ, qv);
-            else tmem_st_x16(tQ, qv);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(Q_QTM));
-        }
         const float sl2 = a.scale * LOG2E;
         float lse2 = 0.f, dlt = 0.f;
         if (valid) {
@@ -862,10 +842,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int D>
 int launch_bwd_d(const BwdPtrs &p, BwdArgs a, cudaStream_t st)
 {
-    CUtensorMap mk, mv, mdo, mq64, mdo64;
+    CUtensorMap mk, mv, mdo, mq, mq64, mdo64;
     const int R = a.layout == CP_LAYOUT_STRIPED ? a.N : 1;
     if (!make_map(&mk, p.k, a.B, a.S, a.Hkv, D, 128, R) || !make_map(&mv, p.v, a.B, a.S, a.Hkv, D, 128, R) ||
-        !make_map(&mdo, p.dout, a.B, a.S, a.Hq, D, 128, R) ||
+        !make_map(&mdo, p.dout, a.B, a.S, a.Hq, D, 128, R) || !make_map(&mq, p.q, a.B, a.S, a.Hq, D, 128, R) ||
         !make_map(&mq64, p.q, a.B, a.S, a.Hq, D, 64, R) || !make_map(&mdo64, p.dout, a.B, a.S, a.Hq, D, 64, R))
         return CP_ECUDA;
     static bool attr_done[64] = {};
@@ -898,7 +878,7 @@ int launch_bwd_d(const BwdPtrs &p, BwdArgs a, cudaStream_t st)
     const int64_t kunits = (int64_t)g.N * g.cpr * a.tpc * a.B * a.Hkv;
     if (qunits > 0x7fffffffLL || kunits > 0x7fffffffLL) return CP_EUNSUPPORTED;
     bwd_dq_kernel<D><<<(unsigned)qunits, NTHREADS, DqCfg<D>::SMEM, st>>>(
-        mk, mv, mdo, a, static_cast<const __nv_bfloat16 *>(p.q), p.lse, delta,
+        mq, mk, mv, mdo, a, p.lse, delta,
         static_cast<__nv_bfloat16 *>(p.dq));
     if (cudaGetLastError() != cudaSuccess) return CP_ECUDA;
     bwd_dkdv_kernel<D><<<(unsigned)kunits, NTHREADS, DkvCfg<D>::SMEM, st>>>(
