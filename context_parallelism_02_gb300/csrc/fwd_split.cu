@@ -136,6 +136,10 @@ int fwd_split_choose(int B, int Hq, int S, int D, int N, int causal, int layout,
     const Geom g = make_geom(S, N, layout, causal);
     const int upc = (g.clen + 127) / 128;
     const int nch = num_selected_chunks(g, rank_lo, rank_hi);
+    const bool grouped = rank_lo == 0 && rank_hi == N;
+    const int64_t units = (int64_t)nch * upc * B * Hq;
+    // no split is a candidate (too many blocks already): skip the simulation
+    if (max_split < 2 || units * 2 > 64LL * num_sms) return 1;
     std::vector<int> tiles((size_t)nch * upc);
     for (int cu = 0; cu < nch; ++cu) {
         const int ch = selected_chunk(g, rank_lo, rank_hi, cu);
@@ -146,8 +150,6 @@ int fwd_split_choose(int B, int Hq, int S, int D, int N, int causal, int layout,
             tiles[(size_t)cu * upc + pu] = KvIter<256>::count(g, chunk_rank(g, ch), last - 1);
         }
     }
-    const bool grouped = rank_lo == 0 && rank_hi == N;
-    const int64_t units = (int64_t)nch * upc * B * Hq;
     const int64_t rows = (int64_t)B * nch * g.clen * Hq;
     const double tile_s = D == 128 ? 1.45e-6 : 1.1e-6;
     static const int cand[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 20, 24, 32};
