@@ -74,8 +74,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, dev_index, uuid=None):
+    def __init__(self, dev_index, uuid=None, period_ms=200):
         self.dev = uuid or str(dev_index)
+        self.period_ms = period_ms
         self.proc = None
         self.path = None
 
@@ -85,7 +86,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.dev, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -419,7 +420,10 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     peaks, peak_src = load_peaks()
-    stream = torch.cuda.current_stream()
+    # one ordinary stream for all work of this process (the legacy default
+    # stream would order itself against the end-to-end copy streams)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
 
     # inputs: drawn on the host (seeded), pinned, copied once to HBM
     qh, kh, vh = (t.pin_memory() for t in inputs.make_qkv(w))
@@ -517,11 +521,17 @@ def main():
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # clocks during the end-to-end steps too: the copies share the board's
+    # power budget with the SMs
+    e2e_sampler = ClockSampler(local, getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+                               and "GPU-" + str(torch.cuda.get_device_properties(dev).uuid), 50)
+    e2e_sampler.start()
     t0.record(stream)
     up.wait_event(t0)
     e2e_run(e2e_steps)
     t1.record(stream)
     torch.cuda.synchronize()
+    e2e_clocks = e2e_sampler.stop()
     assert api.cp_get_error() == 0
     e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e2e_steps, world, dev)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
@@ -561,7 +571,7 @@ def main():
         "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "steps": e2e_steps,
-                "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"],
+                "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"], "clocks": e2e_clocks,
                 "note": "pinned host buffers; uploads and read-backs of neighbouring steps "
                         "overlap the forward on two copy streams"},
         "gpu_launches": args.steps,

@@ -26,9 +26,10 @@
 // is written once, and the result is deterministic.
 //
 // Roles of both tensor-core kernels (384 threads, three warpgroups): warp 0
-// TMA producer, warp 1 MMA issuer, warps 2-3 idle, warps 4-7 and 8-11 the two
-// halves (64 columns each) of the elementwise gradient of one 128x128 tile, one
-// thread per tensor-memory lane.  Every wait is bounded.
+// TMA producer (dQ: K tiles; warp 3 loads Q, dO and V), warps 1 and 2 MMA
+// issuers (one thread each), warps 4-7 and 8-11 the elementwise gradient
+// (dQ: the two 64-column halves of one 128x128 tile; dK/dV: one warpgroup per
+// half-step buffer), one thread per tensor-memory lane.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -72,18 +73,6 @@ __device__ __forceinline__ void ss_seq(uint32_t tD, uint64_t dA, uint64_t dB, ui
         constexpr uint32_t ob = (uint32_t)(((KK >> 2) * BOXB + (KK & 3) * 32) >> 4);
         mma_ss_off<oa, ob>(tD, dA, dB, id, KK > 0 ? 1u : 0u);
         ss_seq<KK + 1, D, BOXB>(tD, dA, dB, id);
-    }
-}
-
-// D/16 MMAs M=128, K=16, A (bf16 pairs) from tensor memory columns tA + 8 KK,
-// B K-major in 128-row boxes
-template <int KK, int D>
-__device__ __forceinline__ void tsk_seq(uint32_t tD, uint32_t tA, uint64_t dB, uint32_t id)
-{
-    if constexpr (KK < D / 16) {
-        constexpr uint32_t ob = (uint32_t)(((KK >> 2) * 16384 + (KK & 3) * 32) >> 4);
-        mma_ts_off<ob>(tD, tA + KK * 8, dB, id, KK > 0 ? 1u : 0u);
-        tsk_seq<KK + 1, D>(tD, tA, dB, id);
     }
 }
 
