@@ -517,11 +517,12 @@ enum {
     K_QFULL = 1,                  // K_QST half stages
     K_QEMPTY = 1 + K_QST,         // K_QST half stages
     K_SDP = 1 + 2 * K_QST,        // 2 buffers: S^T, dP^T complete
-    K_PDS = 3 + 2 * K_QST,        // 2 buffers: P^T, dS^T written (4 arrivals: one warpgroup)
+    K_PW = 3 + 2 * K_QST,         // 2 buffers: P^T written (4 arrivals: one warpgroup)
     K_BUF = 5 + 2 * K_QST,        // 2 buffers: dV/dK(s) complete, buffer s%2 may be rewritten
     K_FIN = 7 + 2 * K_QST,
     K_DRAIN = 8 + 2 * K_QST,      // one commit per issuing thread (2)
-    K_NBAR = 9 + 2 * K_QST
+    K_DSW = 9 + 2 * K_QST,        // 2 buffers: dS^T written (4 arrivals)
+    K_NBAR = 11 + 2 * K_QST
 };
 
 template <int D>
@@ -578,7 +579,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(K_SDP + i), 1);
-            mbar_init(BAR(K_PDS + i), 4);
+            mbar_init(BAR(K_PW + i), 4);
+            mbar_init(BAR(K_DSW + i), 4);
             mbar_init(BAR(K_BUF + i), 1);
         }
         mbar_init(BAR(K_FIN), 1);
@@ -686,12 +688,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t tDV = tmem + C::TM_DV, tDK = tmem + C::TM_DK;
                 Ring<K_QST> rs;
                 for (int s = 0; ok && s < ns; ++s, rs.next()) {
-                    if (!wait1(BAR(K_PDS + (s & 1)), (s >> 1) & 1, wc)) break;
+                    if (!wait1(BAR(K_PW + (s & 1)), (s >> 1) & 1, wc)) break;
                     tc_fence_after();
                     const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
                     const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
-                    // dV += P^T dO_s, dK += dS^T Q_s (K = 64 queries: 4 MMAs each)
+                    // dV += P^T dO_s as soon as P^T is written, while the gradient
+                    // warps compute dS^T; then dK += dS^T Q_s (K = 64 queries: 4 MMAs each)
                     ts_mn_seq<0, 4, 0>(tDV, tb, dQmn0 + so + (uint64_t)(HB >> 4), idKV, s > 0 ? 1u : 0u);
+                    if (!wait1(BAR(K_DSW + (s & 1)), (s >> 1) & 1, wc)) break;
+                    tc_fence_after();
                     ts_mn_seq<0, 4, 0>(tDK, tb + 64u, dQmn0 + so, idKV, s > 0 ? 1u : 0u);
                     // S^T/dP^T(s) completed before the gradient warps started, so the
                     // stage is free once dV/dK(s) completes
@@ -772,6 +777,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     pp[2 * e4 + 1] = pack_bf16(p2, p3);
                 }
                 tmem_st_x32(tb, pp);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(K_PW + half));   // dV(s) may start
             }
             {
                 // dS^T = P^T (dP^T - Delta)
@@ -793,7 +802,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(K_PDS + half));
+            if (lane == 0) mbar_arrive(BAR(K_DSW + half));
         }
         if (ok && waitw(BAR(K_FIN), 0, wc)) {
             tc_fence_after();
