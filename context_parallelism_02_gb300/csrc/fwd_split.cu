@@ -33,8 +33,8 @@ namespace {
 template <int D>
 __global__ void __launch_bounds__(256) split_combine_kernel(const float4 *__restrict__ po,
                                                             const float *__restrict__ pl, int ns,
-                                                            int64_t pstride, Geom g, int B, int Hq,
-                                                            int lo, int hi, int64_t rows,
+                                                            int64_t pstride, Geom g, int Hq, int lo,
+                                                            int hi, int64_t rows,
                                                             __nv_bfloat16 *__restrict__ out,
                                                             float *__restrict__ lse)
 {
@@ -45,7 +45,6 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const float4 *__rest
     const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t nsel = (int64_t)num_selected_chunks(g, lo, hi) * g.clen;   // slots per batch
-    (void)B;
     for (int64_t r = wid * RPW + sub; r < rows; r += nw * RPW) {
         const int h = (int)(r % Hq);
         const int64_t rest = r / Hq;
@@ -115,11 +114,11 @@ int launch_fwd_split_combine(const FwdArgs &a, const SplitOut &so, void *out, fl
     const float4 *po = reinterpret_cast<const float4 *>(so.out);
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
     if (a.D == 128)
-        split_combine_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(po, so.lse, so.n, pstride, g, a.B,
-                                                                    a.Hq, a.rank_lo, a.rank_hi, rows, o, lse);
+        split_combine_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(po, so.lse, so.n, pstride, g, a.Hq,
+                                                                    a.rank_lo, a.rank_hi, rows, o, lse);
     else if (a.D == 64)
-        split_combine_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(po, so.lse, so.n, pstride, g, a.B,
-                                                                   a.Hq, a.rank_lo, a.rank_hi, rows, o, lse);
+        split_combine_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(po, so.lse, so.n, pstride, g, a.Hq,
+                                                                   a.rank_lo, a.rank_hi, rows, o, lse);
     else
         return CP_EUNSUPPORTED;
     return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
