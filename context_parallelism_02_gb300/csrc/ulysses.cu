@@ -10,8 +10,10 @@
 //
 // The unit of copying is a run of H/N heads x D elements, contiguous on both
 // sides.  Runs are numbered in the order of the side that is read, so reads
-// are fully sequential; each thread moves four vectors (16 bytes when sizes
-// and pointers allow) per iteration, loads before stores.  HBM-bound: bytes moved = 2 x tensor bytes.
+// are fully sequential, in vectors of 16 bytes when sizes and pointers allow.
+// Runs of at least 8 vectors go through the group kernel, which resolves a
+// run's destination once per warp and group; shorter runs through a kernel
+// that resolves it per vector.  HBM-bound: bytes moved = 2 x tensor bytes.
 #include <cuda_runtime.h>
 
 #include "cp_common.cuh"
@@ -96,9 +98,70 @@ __global__ void __launch_bounds__(256) ulysses_kernel(const V *__restrict__ src,
     }
 }
 
+// Each warp moves groups of 256 consecutive source vectors (8 per lane, 32
+// apart: coalesced, all loads before the stores).  The destination of a run
+// is computed once per group, by the lane that owns the run, and handed to
+// the lanes that store into it by a warp shuffle; a lane's run and offset
+// advance by additions from its first vector.  With at least 8 vectors per
+// run a group spans at most 32 runs (one per lane).
+template <typename V, bool TO_HEAD, typename I>
+__global__ void __launch_bounds__(256) ulysses_group_kernel(const V *__restrict__ src,
+                                                            V *__restrict__ dst, UlyArgs u)
+{
+    constexpr int VPL = 8, GV = 32 * VPL;
+    const int lane = threadIdx.x & 31;
+    const I total = (I)u.total;
+    const I rv = (I)u.run_vecs;
+    const I nrun = total / rv;
+    const I wid = ((I)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const I nw = ((I)gridDim.x * blockDim.x) >> 5;
+    for (I g0 = wid * GV; g0 < total; g0 += nw * GV) {
+        V val[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const I v = g0 + (I)(lane + 32 * k);
+            if (v < total) val[k] = src[v];
+        }
+        const I r0 = g0 / rv;                        // first run of the group
+        const I rj = r0 + (I)lane;                   // the run this lane resolves
+        const I dj = rj < nrun ? dest_run<TO_HEAD, I>(u, rj) : (I)0;
+        const I first = g0 - r0 * rv + (I)lane;      // offset of this lane's first vector from run r0
+        int q = (int)(first / rv);
+        I rem = first - (I)q * rv;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const I d = __shfl_sync(0xffffffffu, dj, q);
+            const I v = g0 + (I)(lane + 32 * k);
+            if (v < total) dst[d * rv + rem] = val[k];
+            rem += 32;
+            while (rem >= rv) {
+                rem -= rv;
+                ++q;
+            }
+        }
+    }
+}
+
 template <typename V>
 int launch_v(const void *src, void *dst, const UlyArgs &u, int to_head, cudaStream_t st)
 {
+    if (u.run_vecs >= 8) {
+        int64_t blocks = (u.total + 2047) / 2048;    // 8 warps x 256 vectors per block
+        const int64_t cap = (int64_t)sm_count() * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) return CP_OK;
+        const bool small = u.total < 0x7fffffffLL - 4096 && (int64_t)u.B * u.g.S * u.g.N < 0x7fffffffLL;
+        const V *s = (const V *)src;
+        V *d = (V *)dst;
+        if (small) {
+            if (to_head) ulysses_group_kernel<V, true, uint32_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+            else ulysses_group_kernel<V, false, uint32_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+        } else {
+            if (to_head) ulysses_group_kernel<V, true, int64_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+            else ulysses_group_kernel<V, false, int64_t><<<(unsigned)blocks, 256, 0, st>>>(s, d, u);
+        }
+        return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
+    }
     int64_t blocks = (u.total + 1023) / 1024;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
