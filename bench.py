@@ -526,14 +526,20 @@ def main():
     e2e_sampler = ClockSampler(local, getattr(torch.cuda.get_device_properties(dev), "uuid", None)
                                and "GPU-" + str(torch.cuda.get_device_properties(dev).uuid), 50)
     e2e_sampler.start()
-    t0.record(stream)
-    up.wait_event(t0)
-    e2e_run(e2e_steps)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    # three repetitions of the pipelined steps, each with all its copies inside
+    # its own timed region; the median is reported (the host side of the box
+    # is shared, and one repetition can catch a stall there)
+    e2e_all = []
+    for _ in range(3):
+        t0.record(stream)
+        up.wait_event(t0)
+        e2e_run(e2e_steps)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        e2e_all.append(t0.elapsed_time(t1) / e2e_steps)
     e2e_clocks = e2e_sampler.stop()
     assert api.cp_get_error() == 0
-    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / e2e_steps, world, dev)
+    e2e_ms = max_over_ranks(statistics.median(e2e_all), world, dev)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
     # the host link alone (one upload, one read-back, nothing else running): the
@@ -570,7 +576,7 @@ def main():
         "clocks": clocks,
         "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "steps": e2e_steps,
+                "steps": e2e_steps, "repetitions_ms_per_step": e2e_all,
                 "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"], "clocks": e2e_clocks,
                 "note": "pinned host buffers; uploads and read-backs of neighbouring steps "
                         "overlap the forward on two copy streams"},
