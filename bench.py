@@ -132,6 +132,25 @@ def clocks_rejected(c):
 _QKV_CACHE = {}
 
 
+def oracle_per_config():
+    """The fp64 oracle on the other forward workloads: the tiny one and S=8192
+    in full, the GQA S=32768 one on a row sample (seconds each)."""
+    import oracle
+    from context_parallelism_02_gb300 import inputs
+    oracle.build()
+    res = {}
+    for w in (inputs.TINY, inputs.S8K):
+        q, k, v = inputs.make_qkv(w)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, w.causal)
+        dt = time.perf_counter() - t0
+        res[w.name] = {"s": dt, "TFLOP/s": fwd_flops(w) / dt / 1e12, "rows": "all"}
+    w = inputs.GQA32K
+    tf, dt, n, _ = oracle_sample_rows(w, target_s=3.0)
+    res[w.name] = {"s": dt, "TFLOP/s": tf, "rows": f"{n} random query rows x {w.Hq} heads"}
+    return res
+
+
 def oracle_sample_rows(w, target_s, seed=0):
     """Time the fp64 oracle on a bounded sample of query rows of the workload.
 
@@ -219,6 +238,27 @@ def extras(dev, stream, peaks):
     from context_parallelism_02_gb300 import api, inputs
     hbm = peaks["hbm_gbs"]
     out = {}
+    # the other forward workloads of the scope table: tiny fp32 (S=512, D=64,
+    # N=4), S=8192 (H=8, N=8) and GQA S=32768 (Hq=32, Hkv=8, N=8), zigzag, causal
+    cfgs = {}
+    for w in (inputs.TINY, inputs.S8K, inputs.GQA32K):
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        q = torch.randn(w.B, w.S, w.Hq, w.D, device=dev, generator=g).to(w.dtype)
+        k, v = (torch.randn(w.B, w.S, w.Hkv, w.D, device=dev, generator=g).to(w.dtype) for _ in range(2))
+        o = torch.empty_like(q)
+        lo = torch.empty(w.B, w.Hq, w.S, device=dev)
+        f = lambda: api.ring_attn_fwd(q, k, v, w.N, w.layout, w.causal, out=o, lse=lo, stream=stream)
+        for _ in range(3):
+            f()
+        ms = time_events(f, 20, stream)
+        tf = fwd_flops(w) / ms / 1e9
+        entry = {"dtype": str(w.dtype).replace("torch.", ""), "ms": ms, "TFLOP/s": tf,
+                 "masked_in_flops": fwd_flops(w)}
+        if w.dtype == torch.bfloat16:
+            entry["frac_bf16_burst"] = tf / peaks["bf16_tflops"]
+        cfgs[w.name] = entry
+        del q, k, v, o, lo
+    out["configs_fwd"] = cfgs
     # lse_merge: rows = 1x8x131072, D = 128, fp32 partials
     a, la, b, lb = (t.to(dev) for t in inputs.make_merge_inputs())
     o = torch.empty_like(a)
@@ -598,7 +638,8 @@ def main():
         line["cpu_baseline"] = {
             "value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} random query rows x {w.Hq} heads of the workload ({dt:.1f} s, "
-                      f"fp64, OpenMP); masked-in FLOPs of the sample counted exactly"}
+                      f"fp64, OpenMP); masked-in FLOPs of the sample counted exactly",
+            "per_config": oracle_per_config()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
