@@ -303,6 +303,30 @@ def extras(dev, stream, peaks):
     res["bytes"] = nb
     out["ulysses_q_gqa32k"] = res
     del x, y, x2
+    # USP on the GQA workload: n_ulysses x n_ring = 8 virtual ranks, each grid
+    # against the plain ring over 8 ranks (relayouts included in the time)
+    w = inputs.GQA32K
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    q = torch.randn(w.B, w.S, w.Hq, w.D, device=dev, generator=g).to(torch.bfloat16)
+    k, v = (torch.randn(w.B, w.S, w.Hkv, w.D, device=dev, generator=g).to(torch.bfloat16) for _ in range(2))
+    o = torch.empty_like(q)
+    lo = torch.empty(w.B, w.Hq, w.S, device=dev)
+    usp = {}
+    for nu in (1, 2, 4, 8):
+        nr = 8 // nu
+        if nu == 1:
+            f = lambda: api.ring_attn_fwd(q, k, v, nr, w.layout, True, out=o, lse=lo, stream=stream)
+        else:
+            ws = torch.empty(api._lib.load().usp_attn_fwd_workspace(w.Hq, w.Hkv, w.S, w.D, 1),
+                             dtype=torch.uint8, device=dev)
+            f = lambda: api.usp_attn_fwd(q, k, v, nu, nr, w.layout, True, out=o, lse=lo,
+                                         workspace=ws, stream=stream)
+        for _ in range(3):
+            f()
+        ms = time_events(f, 10, stream)
+        usp[f"{nu}x{nr}"] = {"ms": ms, "TFLOP/s": fwd_flops(w) / ms / 1e9}
+    out["usp_gqa32k"] = {"grid": "n_ulysses x n_ring (1 x 8 is the plain ring)", **usp}
+    del q, k, v, o, lo
     # per-rank work and time, long workload, contiguous vs zigzag vs striped
     w = inputs.LONG128K
     g = torch.Generator(device=dev).manual_seed(w.seed)
