@@ -432,6 +432,61 @@ def extras(dev, stream, peaks):
     return out
 
 
+def _r(x, sig=4):
+    return float(f"{x:.{sig}g}") if isinstance(x, float) and math.isfinite(x) else x
+
+
+def rounded(obj):
+    """Floats to 4 significant digits (keeps the JSON line short)."""
+    if isinstance(obj, dict):
+        return {k: rounded(v) for k, v in obj.items()}
+    if isinstance(obj, (list, tuple)):
+        return [rounded(v) for v in obj]
+    return _r(obj)
+
+
+def compact_extras(full):
+    """Scalar summaries of the extras: per-rank arrays become max/mean ratios."""
+    c = {}
+    for name, e in full.get("configs_fwd", {}).items():
+        c[f"fwd_{name.split('_')[0]}_ms"] = e["ms"]
+        c[f"fwd_{name.split('_')[0]}_TFLOPs"] = e["TFLOP/s"]
+    b = full.get("ring_attn_bwd_bwd32k")
+    if b:
+        c["bwd32k_ms"] = b["ms"]
+        c["bwd32k_TFLOPs_alg"] = b["TFLOP/s"]
+        c["bwd32k_frac_burst"] = b["frac_bf16_burst"]
+    for lay, e in full.get("per_rank_long128k", {}).items():
+        c[f"long128k_{lay}_ms"] = e["ms_all_ranks"]
+        c[f"long128k_{lay}_rank_time_max_over_mean"] = e["time_max_over_mean"]
+        c[f"long128k_{lay}_rank_work_max_over_mean"] = e["work_max_over_mean"]
+        c[f"long128k_{lay}_slowest_rank_ms_unsplit_split"] = e["split_max_rank_ms_vs_unsplit"][::-1]
+    sk = full.get("split_kv_one_head_long128k")
+    if sk:
+        c["split_1head_slowest_rank_ms_unsplit_split"] = [sk["max_rank_ms_unsplit"],
+                                                          sk["max_rank_ms_split"]]
+    u = full.get("usp_gqa32k")
+    if u:
+        c["usp_gqa32k_ms"] = {k: v["ms"] for k, v in u.items() if isinstance(v, dict)}
+    for key in ("ring_steps_long128k",):
+        if key in full:
+            c[key] = full[key]
+    return c
+
+
+def hbm_summary(full, peaks):
+    out = {"peak_GBs": peaks["hbm_gbs"]}
+    for key, name in (("lse_merge", "lse_merge"), ("lse_merge_n4", "lse_merge_n4")):
+        if key in full:
+            out[name] = {"GB/s": full[key]["GB/s"], "frac_hbm": full[key]["frac_hbm"]}
+    u = full.get("ulysses_q_gqa32k")
+    if u:
+        for d in ("seq_to_head", "head_to_seq"):
+            out[f"ulysses_{d}"] = {"GB/s": u[d]["GB/s"], "frac_hbm": u[d]["frac_hbm"]}
+        out["ulysses_roundtrip_bit_exact"] = u["bit_exact_roundtrip"]
+    return out
+
+
 # ----------------------------------------------------------------------------- ranks
 
 def max_over_ranks(x, world, device):
@@ -461,6 +516,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=6.0)
+    ap.add_argument("--extras-full", action="store_true",
+                    help="print every per-rank array of the extras (a long line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -593,8 +650,16 @@ def main():
     # three repetitions of the pipelined steps, each with all its copies inside
     # its own timed region; the median is reported (the host side of the box
     # is shared, and one repetition can catch a stall there)
-    e2e_all = []
+    e2e_all, fwd_only_all = [], []
     for _ in range(3):
+        # the same forward with inputs already in HBM, timed right before the
+        # end-to-end steps, so both see the same clocks and power state
+        t0.record(stream)
+        for _ in range(e2e_steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        fwd_only_all.append(t0.elapsed_time(t1) / e2e_steps)
         t0.record(stream)
         up.wait_event(t0)
         e2e_run(e2e_steps)
@@ -604,6 +669,7 @@ def main():
     e2e_clocks = e2e_sampler.stop()
     assert api.cp_get_error() == 0
     e2e_ms = max_over_ranks(statistics.median(e2e_all), world, dev)
+    fwd_only_ms = max_over_ranks(statistics.median(fwd_only_all), world, dev)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
     # the host link alone (one upload, one read-back, nothing else running): the
@@ -640,10 +706,18 @@ def main():
         "clocks": clocks,
         "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "steps": e2e_steps, "repetitions_ms_per_step": e2e_all,
-                "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"], "clocks": e2e_clocks,
+                "steps": e2e_steps,
+                "fwd_only_ms_per_step": fwd_only_ms,
+                "e2e_over_fwd_only": e2e_ms / fwd_only_ms,
+                "rep_ms_min": min(e2e_all), "rep_ms_max": max(e2e_all),
+                "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"],
+                "copy_ms_per_step": h2d / link["h2d"] / 1e6 + d2h / link["d2h"] / 1e6,
+                "sm_mhz": e2e_clocks.get("sm_mhz"),
+                "power_w_max": e2e_clocks.get("power_w_max"),
+                "reasons": ",".join(e2e_clocks.get("reasons", [])),
                 "note": "pinned host buffers; uploads and read-backs of neighbouring steps "
-                        "overlap the forward on two copy streams"},
+                        "overlap the forward on two copy streams; fwd_only_ms_per_step is the "
+                        "device-only forward timed just before each repetition (same clocks)"},
         "gpu_launches": args.steps,
     }
     if remeasured:
@@ -655,15 +729,26 @@ def main():
         if tr.get("workload") == args.workload and tr.get("kernel_source_sha") == kernel_sha():
             line["roofline"]["traffic"] = tr["bytes_per_launch"]
 
+    full = None
     if rank == 0 and world == 1 and not args.no_extras:
-        line["extras"] = extras(dev, stream, peaks)
+        full = extras(dev, stream, peaks)
+        line["extras"] = full if args.extras_full else compact_extras(full)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, n, cores = oracle_sample_rows(w, target_s=12.0)
         line["cpu_baseline"] = {
             "value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} random query rows x {w.Hq} heads of the workload ({dt:.1f} s, "
-                      f"fp64, OpenMP); masked-in FLOPs of the sample counted exactly",
-            "per_config": oracle_per_config()}
+                      f"fp64, OpenMP); masked-in FLOPs of the sample counted exactly"}
+        if args.extras_full:
+            line["cpu_baseline"]["per_config"] = oracle_per_config()
+    if full is not None:
+        # the HBM-bound kernels last, so that they survive any truncation of the
+        # line from the front
+        line["hbm_kernels"] = rounded(hbm_summary(full, peaks))
+    if "extras" in line:
+        line["extras"] = rounded(line["extras"])
+    keep = {k: line["e2e"][k] for k in ("value", "ms_per_step")}
+    line["e2e"] = {**rounded(line["e2e"]), **keep}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -17,6 +17,8 @@ CP_EHEADS = -2
 CP_EUNSUPPORTED = -3
 CP_ECUDA = -4
 CP_ETIMEOUT = -5
+CP_ESMEM = -6
+CP_EBOUNDS = -7
 
 CP_LAYOUT_CONTIGUOUS = 0
 CP_LAYOUT_ZIGZAG = 1

@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     if (base & 1023u) {   // the 128B-swizzled tiles need 1 KB alignment
-        if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_TIMEOUT);
+        if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_SMEM_ALIGN);
         return;
     }
     const uint32_t sDO = base + C::OFF_DO, sQ = base + C::OFF_Q, sK = base + C::OFF_K,
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     if (base & 1023u) {   // the 128B-swizzled tiles need 1 KB alignment
-        if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_TIMEOUT);
+        if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_SMEM_ALIGN);
         return;
     }
     const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQ = base + C::OFF_Q,

@@ -27,6 +27,8 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "cp.h"
 #include "kernels.h"
 
@@ -58,20 +60,14 @@ float *scratch_ptr()
 
 bool al16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-}  // namespace
-
-}  // namespace cp
-
-using namespace cp;
-
-extern "C" int ring_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *out,
-                                     const float *lse, const void *dout, void *dq, void *dk,
-                                     void *dv, int B, int Hq, int Hkv, int64_t S, int D, int N,
-                                     int causal, int layout, int dtype, float scale, void *stream)
+int noalloc_impl(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                 const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int64_t S,
+                 int D, int N, int causal, int layout, int dtype, float scale, void *stream)
 {
     if (B < 0 || Hq < 1 || Hkv < 1 || N < 1 || S < 0 || S > 0x7fffffffLL) return CP_EINVAL;
     if (causal != 0 && causal != 1) return CP_EINVAL;
-    if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_ZIGZAG) return CP_EINVAL;
+    if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_ZIGZAG && layout != CP_LAYOUT_STRIPED)
+        return CP_EINVAL;
     if (S % N || (layout == CP_LAYOUT_ZIGZAG && S % (2 * (int64_t)N))) return CP_EINVAL;
     if (Hq % Hkv) return CP_EINVAL;
     if (dtype != CP_BF16) return CP_EUNSUPPORTED;
@@ -103,4 +99,22 @@ extern "C" int ring_attn_bwd_noalloc(const void *q, const void *k, const void *v
     a.limit_ns = device_wait_limit_ns();
     BwdPtrs p{q, k, v, out, lse, dout, dq, dk, dv, scratch};
     return launch_bwd_bf16(p, a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+}  // namespace cp
+
+using namespace cp;
+
+extern "C" int ring_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *out,
+                                     const float *lse, const void *dout, void *dq, void *dk,
+                                     void *dv, int B, int Hq, int Hkv, int64_t S, int D, int N,
+                                     int causal, int layout, int dtype, float scale, void *stream)
+{
+    nvtxRangePushA("ring_attn_bwd_noalloc");
+    const int rc = noalloc_impl(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, N, causal,
+                                layout, dtype, scale, stream);
+    nvtxRangePop();
+    return rc;
 }

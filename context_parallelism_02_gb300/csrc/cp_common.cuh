@@ -46,7 +46,9 @@
 namespace cp {
 
 // Error word values (per device, read and cleared by cp_get_error).
-constexpr unsigned ERRW_TIMEOUT = 1u;
+constexpr unsigned ERRW_TIMEOUT = 1u;       // a bounded wait ran out
+constexpr unsigned ERRW_SMEM_ALIGN = 2u;    // dynamic shared memory not 1 KB aligned
+constexpr unsigned ERRW_BOUNDS = 3u;        // debug-bounds build: tile coordinate out of range
 
 // All positions are int32: the library rejects S > INT32_MAX, and 32-bit
 // index arithmetic keeps the kernels free of 64-bit division routines.

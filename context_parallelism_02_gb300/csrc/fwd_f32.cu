@@ -1,4 +1,4 @@
-// fwd_f32.cu -- fp32 ring-attention forward on the FFMA pipes.
+// fwd_f32.cu -- fp32 ring-attention forward on the CUDA cores (fp64 arithmetic).
 //
 // The fp32 path has to agree with an fp64 reference to ~1e-5 even with
 // logits of several tens (q scaled by 8), which rules out the tf32

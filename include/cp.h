@@ -54,6 +54,10 @@ extern "C" {
 #define CP_EUNSUPPORTED (-3)  /* dtype / head dim / shape combination not built */
 #define CP_ECUDA (-4)         /* a CUDA runtime call or launch failed */
 #define CP_ETIMEOUT (-5)      /* a device-side bounded wait ran out (cp_get_error) */
+#define CP_ESMEM (-6)         /* a kernel's dynamic shared memory base was not 1 KB aligned
+                                 (cp_get_error); the kernel returned without work */
+#define CP_EBOUNDS (-7)       /* debug-bounds build only: an out-of-range tile coordinate was
+                                 met and skipped (cp_get_error) */
 
 /* sequence layouts */
 #define CP_LAYOUT_CONTIGUOUS 0
@@ -103,7 +107,9 @@ int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_h
  *   lse [B][Hq][S]: device fp32, lse_i = ln sum_j exp(scale * q_i.k_j).
  *   D in {64, 128}; Hq % Hkv == 0; scale <= 0 selects 1/sqrt(D).
  *   CP_BF16 runs tcgen05 tensor-core kernels (bf16 operands, fp32
- *   accumulation); CP_F32 runs an fp32 FFMA kernel.
+ *   accumulation); CP_F32 runs the precision path: fp32 inputs and outputs,
+ *   with scores, the running max and sum and the output accumulated in fp64
+ *   on the CUDA cores.
  * Errors: CP_EINVAL (null pointer, misalignment, B/Hq/Hkv/S/N < 1, S % N,
  * S % 2N for zigzag, Hq % Hkv), CP_EUNSUPPORTED (D or dtype), CP_ECUDA.
  */
@@ -304,8 +310,11 @@ int ring_attn_bwd_noalloc(const void *q, const void *k, const void *v, const voi
 /*
  * cp_get_error -- synchronise `stream`, then read and clear the calling
  * device's error word.  Returns CP_OK, CP_ETIMEOUT (a kernel's bounded wait
- * ran out and the kernel returned early; its outputs are undefined) or
- * CP_ECUDA (the synchronisation itself failed).
+ * ran out and the kernel returned early; its outputs are undefined),
+ * CP_ESMEM (a kernel found its dynamic shared memory misaligned and returned
+ * without work), CP_EBOUNDS (debug-bounds build only) or CP_ECUDA (the
+ * synchronisation itself failed).  The first failure recorded since the last
+ * read wins.
  */
 int cp_get_error(void *stream);
 

@@ -59,3 +59,47 @@ def test_single_rank_identity():
     import bench
     assert bench.max_over_ranks(7.5, 1, "cpu") == 7.5
     assert bench.job_value(2e12, 1, 1000.0) == 2.0
+
+
+def _fake_extras():
+    per = {"n_split_per_rank": [1] * 16, "ms_per_rank_split": [1.0] * 16,
+           "split_max_rank_ms_vs_unsplit": [1.6, 1.7], "masked_in_pairs_per_rank": [4294508544] * 16,
+           "work_max_over_mean": 1.0001144400448605, "ms_per_rank": [1.55] * 16,
+           "time_max_over_mean": 1.0311458828609423, "ms_all_ranks": 23.352884928385418,
+           "TFLOP/s_all_ranks": 1506.6507042785574, "executed_tiles_128x256": 2162688}
+    return {
+        "configs_fwd": {n: {"dtype": "bfloat16", "ms": 0.1331, "TFLOP/s": 1031.2, "masked_in_flops": 1}
+                        for n in ("tiny_s512_d64_n4", "s8192_h8_d128_n8_zigzag_causal",
+                                  "gqa_s32768_hq32_hkv8_d128_n8_zigzag_causal")},
+        "lse_merge": {"rows": 1, "D": 128, "bytes": 1, "ms": 0.25, "GB/s": 6419.123, "frac_hbm": 0.9461},
+        "lse_merge_n4": {"rows": 1, "D": 128, "n": 4, "bytes": 1, "ms": 0.43, "GB/s": 6233.1,
+                         "frac_hbm": 0.92},
+        "ulysses_q_gqa32k": {"seq_to_head": {"ms": 1.0, "GB/s": 6337.0, "frac_hbm": 0.934},
+                             "head_to_seq": {"ms": 1.0, "GB/s": 6362.0, "frac_hbm": 0.94},
+                             "bit_exact_roundtrip": True, "bytes": 1},
+        "usp_gqa32k": {"grid": "n_ulysses x n_ring", **{k: {"ms": 5.8, "TFLOP/s": 1500.0}
+                                                         for k in ("1x8", "2x4", "4x2", "8x1")}},
+        "per_rank_long128k": {lay: dict(per) for lay in ("contiguous", "zigzag", "striped")},
+        "split_kv_one_head_long128k": {"max_rank_ms_unsplit": 0.87, "max_rank_ms_split": 0.29},
+        "ring_attn_bwd_bwd32k": {"ms": 24.29, "TFLOP/s": 905.13, "frac_bf16_burst": 0.4823,
+                                 "executed_TFLOP/s": 1267.18},
+    }
+
+
+def test_compact_line_fits_the_kept_output():
+    """The default bench line (extras as scalar summaries, HBM kernels last)
+    stays well under the ~3 KB of stdout a caller's log tail keeps."""
+    import json
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"hbm_gbs": 6785.2, "bf16_tflops": 1940.6, "bf16_tflops_sustained": 1736.5}
+    full = _fake_extras()
+    line = {"metric": bench.METRIC, "value": 1605.7175086641482, "unit": "TFLOP/s",
+            "extras": bench.rounded(bench.compact_extras(full)),
+            "hbm_kernels": bench.rounded(bench.hbm_summary(full, peaks))}
+    text = json.dumps(line)
+    assert len(text) < 2000, len(text)
+    assert text.index('"hbm_kernels"') > text.index('"extras"')
+    assert line["hbm_kernels"]["lse_merge"]["frac_hbm"] == 0.9461
+    assert line["extras"]["long128k_zigzag_rank_time_max_over_mean"] == 1.031
