@@ -38,6 +38,8 @@ SIGNATURES = {
     "ring_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _P]),
     "ring_attn_fwd_rank": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _I,
                                 _I, _P]),
+    "flash_block_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _I,
+                              _I, _F, _I, _P]),
     "ring_attn_fwd_split": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _L, _I, _I, _I, _I, _I, _F, _I,
                                  _I, _I, _P, ctypes.c_size_t, _P]),
     "ring_attn_fwd_split_workspace": (ctypes.c_size_t, [_I, _I, _L, _I, _I]),

@@ -88,6 +88,48 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, N: int, lay
     return out, lse
 
 
+def flash_block_step(q, k, v, rank: int, source: int, N: int, S: int, layout: int,
+                     causal: bool = True, scale: float | None = None, out_acc=None, lse_acc=None,
+                     out_final=None, accumulate: bool = True, stream=None):
+    """One ring step on shard-local buffers: rank ``rank``'s queries against the
+    KV block of rank ``source``, merged into the running state; returns
+    (out_acc, lse_acc).
+
+    q ``[B, C, Hq, D]`` and k/v ``[B, C, Hkv, D]`` (C = S / N) are in the local
+    row order of their ranks (``cp_shard_map``); out_acc ``[B, C, Hq, D]`` and
+    lse_acc ``[B, Hq, C]`` are fp32 (allocated when None, which requires
+    ``accumulate=False``).  ``out_final`` (optional, q's dtype) receives the
+    merged output rounded to that dtype.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(name, t)
+    if q.dtype not in _DT or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share dtype float32 or bfloat16")
+    B, C, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if (out_acc is None or lse_acc is None) and accumulate:
+        raise ValueError("accumulate=True needs the running state out_acc and lse_acc")
+    if out_acc is None:
+        out_acc = torch.empty((B, C, Hq, D), dtype=torch.float32, device=q.device)
+    if lse_acc is None:
+        lse_acc = torch.empty((B, Hq, C), dtype=torch.float32, device=q.device)
+    for name, t in (("out_acc", out_acc), ("lse_acc", lse_acc)):
+        _need_cuda_contig(name, t)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    if out_final is not None:
+        _need_cuda_contig("out_final", out_final)
+        if out_final.dtype != q.dtype:
+            raise ValueError("out_final must have q's dtype")
+    sc = -1.0 if scale is None else float(scale)
+    rc = _lib.load().flash_block_step(_ptr(q), _ptr(k), _ptr(v), _ptr(out_acc), _ptr(lse_acc),
+                                      _ptr(out_final), B, Hq, Hkv, S, D, N, rank, source,
+                                      int(causal), layout, _DT[q.dtype], sc, int(accumulate),
+                                      ctypes.c_void_p(_stream(stream)))
+    check(rc, "flash_block_step")
+    return out_acc, lse_acc
+
+
 def cp_fwd_split_count(B: int, Hq: int, S: int, D: int, N: int, layout: int, causal: bool = True,
                        rank_range: tuple[int, int] | None = None, num_sms: int | None = None) -> int:
     """Number of splits for :func:`ring_attn_fwd_split` (host-side dispatch

@@ -236,6 +236,34 @@ int ring_attn_fwd_rank(const void *q, const void *k, const void *v, void *out, f
                       rank_lo, rank_hi, stream);
 }
 
+int flash_block_step(const void *q, const void *k, const void *v, float *out_acc, float *lse_acc,
+                     void *out_final, int B, int Hq, int Hkv, int64_t S, int D, int N, int rank,
+                     int source, int causal, int layout, int dtype, float scale, int accumulate,
+                     void *stream)
+{
+    NvtxScope nvtx_("flash_block_step");
+    if (N < 1 || rank < 0 || rank >= N || source < 0 || source >= N) return CP_EINVAL;
+    if (accumulate != 0 && accumulate != 1) return CP_EINVAL;
+    FwdArgs a;
+    const int rc = prepare_fwd(q, k, v, out_acc, lse_acc, B, Hq, Hkv, S, D, N, causal, layout,
+                               dtype, scale, rank, rank + 1, a);
+    if (rc) return rc == 1 ? CP_OK : rc;
+    if (out_final && !aligned16(out_final)) return CP_EINVAL;
+    a.err = err_ptr();
+    if (!a.err) return CP_ECUDA;
+    StepOut so;
+    so.step_k = ((rank - source) % N + N) % N;
+    so.accumulate = accumulate;
+    so.out_acc = out_acc;
+    so.lse_acc = lse_acc;
+    so.out_final = out_final;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == CP_F32)
+        return launch_fwd_f32_step(static_cast<const float *>(q), static_cast<const float *>(k),
+                                   static_cast<const float *>(v), a, so, st);
+    return launch_fwd_bf16_step(q, k, v, a, so, st);
+}
+
 size_t ring_attn_fwd_split_workspace(int B, int Hq, int64_t S, int D, int n_split)
 {
     if (B < 0 || Hq < 0 || S < 0 || S > 0x7fffffffLL || (D != 64 && D != 128) || n_split < 1 ||

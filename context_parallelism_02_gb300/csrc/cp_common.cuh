@@ -121,6 +121,16 @@ CP_HD int ring_source(int N, int r, int k)
     return s < 0 ? s + N : s;
 }
 
+// Row of slot u in the local order of rank r's shard (u must be held by r):
+// the shard's first chunk is local rows [0, clen), its second (zigzag)
+// [clen, 2 clen).  A shard-local call (flash_block_step) addresses its q, k
+// and v buffers this way.
+CP_HD int slot_lrow(const Geom &g, int r, int u)
+{
+    const int ch = u / g.clen;
+    return (ch == r ? 0 : g.clen) + (u - ch * g.clen);
+}
+
 // Chunks of the ranks [lo, hi), listed by descending global position.  With a
 // causal mask a query's work grows with its position, so walking units in this
 // order hands out the longest work first.
@@ -153,16 +163,20 @@ template <int TILE>
 struct KvIter {
     Geom g;
     int r, qmax;
-    int k, ci;
+    int k, ci, kend;    // ring steps [.., kend) are walked
     int t, nt, cstart, cend;
     int src, shift;     // rank holding the current chunk; diag_shift(r, src)
 
-    CP_HD void begin(const Geom &g_, int r_, int qmax_)
+    // the whole ring: steps 0..N-1
+    CP_HD void begin(const Geom &g_, int r_, int qmax_) { begin_steps(g_, r_, qmax_, 0, g_.N); }
+    // ring steps [k0, k1) only (k1 = k0 + 1: the one block a shard-local step holds)
+    CP_HD void begin_steps(const Geom &g_, int r_, int qmax_, int k0, int k1)
     {
         g = g_;
         r = r_;
         qmax = qmax_;
-        k = 0;
+        k = k0;
+        kend = k1;
         ci = -1;
         t = nt = cstart = cend = src = shift = 0;
         advance_chunk();
@@ -175,7 +189,7 @@ struct KvIter {
                 ci = 0;
                 ++k;
             }
-            if (k >= g.N) return false;
+            if (k >= kend) return false;
             src = ring_source(g.N, r, k);
             shift = diag_shift(g, r, src);
             int ch = rank_chunk(g, src, ci);
@@ -186,11 +200,13 @@ struct KvIter {
             if (nt > 0) return true;
         }
     }
-    CP_HD bool valid() const { return k < g.N; }
+    CP_HD bool valid() const { return k < kend; }
     CP_HD int start() const { return cstart + t * TILE; }
     // tensor-map coordinates of the tile's first key
     CP_HD int mrank() const { return striped(g) ? src : 0; }
     CP_HD int mrow() const { return striped(g) ? t * TILE : start(); }
+    // row of the tile's first key in the source's shard-local buffer
+    CP_HD int lrow() const { return ci * g.clen + t * TILE; }
     CP_HD int len() const
     {
         int l = cend - start();
@@ -210,11 +226,12 @@ struct KvIter {
             if (t >= nt) advance_chunk();
         }
     }
-    // Total tiles of the walk (closed form per chunk).
-    CP_HD static int count(const Geom &g, int r, int qmax)
+    // Total tiles of the walk over ring steps [k0, k1) (closed form per chunk).
+    CP_HD static int count(const Geom &g, int r, int qmax, int k0 = 0, int k1 = -1)
     {
+        if (k1 < 0) k1 = g.N;
         int n = 0;
-        for (int k = 0; k < g.N; ++k) {
+        for (int k = k0; k < k1; ++k) {
             int src = ring_source(g.N, r, k);
             for (int ci = 0; ci < g.cpr; ++ci)
                 n += tiles_needed<TILE>(g, rank_chunk(g, src, ci) * g.clen,

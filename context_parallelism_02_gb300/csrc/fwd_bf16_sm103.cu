@@ -127,16 +127,30 @@ __device__ __forceinline__ void issue_pv_seq(uint32_t tO, uint32_t tP, uint64_t 
 
 // --- the kernel ------------------------------------------------------------------
 
-// SPLIT: the block runs split `sp` of its unit's walk (tiles [j0, j0 + n) of
-// the n_all tiles, cut into so.n nearly equal pieces) and writes the
-// normalised partial (out, lse) of those keys, in fp32, to so.out / so.lse at
-// the row index of the output row: [sp][B][S][Hq][D] and [sp][B][S][Hq].
-template <int D, bool SPLIT>
+// Modes:
+//   MODE_RING   the whole ring over global-order q, k, v; out bf16, lse fp32.
+//   MODE_SPLIT  the block runs split `sp` of its unit's walk (tiles [j0, j0 + n)
+//               of the n_all tiles, cut into so.n nearly equal pieces) and
+//               writes the normalised partial (out, lse) of those keys, in fp32,
+//               to so.out / so.lse at the row index of the output row:
+//               [sp][B][S][Hq][D] and [sp][B][S][Hq].
+//   MODE_STEP   one ring step of one rank on shard-local buffers (the
+//               flash_block of the ring sketch): q is the rank's shard, k and v
+//               the block of the source rank, each in its local row order; the
+//               block's result is merged into the running state (stp.out_acc,
+//               stp.lse_acc) with the log-sum-exp form of the online-softmax
+//               rescaling, and optionally written rounded to bf16.
+enum { MODE_RING = 0, MODE_SPLIT = 1, MODE_STEP = 2 };
+
+template <int D, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a, const float sl2,
-                    __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, const SplitOut so)
+                    __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, const SplitOut so,
+                    const StepOut stp)
 {
+    constexpr bool SPLIT = MODE == MODE_SPLIT;
+    constexpr bool STEP = MODE == MODE_STEP;
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
@@ -168,7 +182,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                        ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, ublk)
                        : decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, ublk);
     const int kvh = w.h / (a.Hq / a.Hkv);
-    const int n_all = KvIter<KT>::count(g, w.r, w.qmax);
+    const int n_all = STEP ? KvIter<KT>::count(g, w.r, w.qmax, stp.step_k, stp.step_k + 1)
+                           : KvIter<KT>::count(g, w.r, w.qmax);
+    const int C_loc = g.clen * g.cpr;   // rows of one shard (MODE_STEP buffers)
     const int j0 = SPLIT ? (int)((int64_t)n_all * sp / so.n) : 0;
     const int n = SPLIT ? (int)((int64_t)n_all * (sp + 1) / so.n) - j0 : n_all;
     if (SPLIT && n == 0) {
@@ -181,6 +197,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int rr = threadIdx.x; rr < rows; rr += NTHREADS)
             so.lse[(((int64_t)sp * a.B + w.b) * a.S + slot_pos(g, w.q0 + rr)) * a.Hq + w.h] = -INFINITY;
+        return;
+    }
+    if (STEP && n == 0) {
+        // no key of this block is visible to the unit: merging changes nothing
+        // (out_final, if asked for, is the state rounded); a first step writes
+        // the empty state (out 0, lse -inf)
+        const int rows = w.qmax - w.q0 + 1;
+        if (stp.accumulate) {
+            if (stp.out_final)
+                for (int i = threadIdx.x; i < rows * (D / 8); i += NTHREADS) {
+                    const int rr = i / (D / 8), c8 = i - rr * (D / 8);
+                    const int64_t orow = ((int64_t)w.b * C_loc + slot_lrow(g, w.r, w.q0 + rr)) * a.Hq + w.h;
+                    const float4 *src = reinterpret_cast<const float4 *>(stp.out_acc + orow * D) + 2 * c8;
+                    const float4 x0 = src[0], x1 = src[1];
+                    reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(stp.out_final) + orow * D)[c8] =
+                        make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
+                                   pack_bf16(x1.z, x1.w));
+                }
+            return;
+        }
+        for (int i = threadIdx.x; i < rows * (D / 4); i += NTHREADS) {
+            const int rr = i / (D / 4), c4 = i - rr * (D / 4);
+            const int64_t orow = ((int64_t)w.b * C_loc + slot_lrow(g, w.r, w.q0 + rr)) * a.Hq + w.h;
+            reinterpret_cast<float4 *>(stp.out_acc + orow * D)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (stp.out_final && c4 < D / 8)
+                reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(stp.out_final) + orow * D)[c4] =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int rr = threadIdx.x; rr < rows; rr += NTHREADS)
+            stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, w.q0 + rr)] = -INFINITY;
         return;
     }
 
@@ -220,12 +266,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // ------------------------------------------------------------ producer
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
             mbar_arrive_expect_tx(BAR(B_Q), C::QBYTES);
+            // map coordinates (rank, row) of the unit's first query
+            const int qmr = STEP ? 0 : slot_mrank(g, w.q0);
+            const int qmw = STEP ? slot_lrow(g, w.r, w.q0) : slot_mrow(g, w.q0);
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, w.h, slot_mrank(g, w.q0),
-                          slot_mrow(g, w.q0), w.b, pol_q);
+                tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, w.h, qmr, qmw, w.b, pol_q);
             // K runs one tile ahead of V; the V loads reuse the K tile starts
             KvIter<KT> itk;
-            itk.begin(g, w.r, w.qmax);
+            if (STEP)
+                itk.begin_steps(g, w.r, w.qmax, stp.step_k, stp.step_k + 1);
+            else
+                itk.begin(g, w.r, w.qmax);
             if (SPLIT) itk.skip(j0);
             int nk = 0, nv = 0;   // tiles whose K / V loads were issued
             int kr_cur = 0, kw_cur = 0, kr_next = 0, kw_next = 0;   // map coordinates (rank, row)
@@ -234,8 +285,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int st = j & 1;
                 if (j >= 2 && !wait1(BAR(B_KEMPTY + st), ((j >> 1) - 1) & 1, wc)) return false;
                 mbar_arrive_expect_tx(BAR(B_KFULL + st), C::KBYTES);
-                kr_next = itk.mrank();
-                kw_next = itk.mrow();
+                kr_next = STEP ? 0 : itk.mrank();
+                kw_next = STEP ? itk.lrow() : itk.mrow();
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load5(sK + st * C::KBYTES + bx * C::KBOX, &tmK, BAR(B_KFULL + st), bx * 64,
                               kvh, kr_next, kw_next, w.b, pol_kv);
@@ -347,7 +398,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool ok = true;
 
         KvIter<KT> it;
-        it.begin(g, w.r, w.qmax);
+        if (STEP)
+            it.begin_steps(g, w.r, w.qmax, stp.step_k, stp.step_k + 1);
+        else
+            it.begin(g, w.r, w.qmax);
         if (SPLIT) it.skip(j0);
         for (int j = 0; j < n; ++j, it.next()) {
             if (!waitw(BAR(B_SFULL), j & 1, wc)) {
@@ -476,6 +530,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (ok && waitw(BAR(B_OFIN), 0, wc)) {
             tc_fence_after();
+            const bool valid = qpos < w.cend;
+            // MODE_STEP: the running lse of the row, read by both halves before
+            // the exchange below (half 0 overwrites it only after the exchange)
+            float prev2 = NEG_INF;
+            int64_t srow = 0;
+            if constexpr (STEP) {
+                srow = ((int64_t)w.b * C_loc + slot_lrow(g, w.r, valid ? qpos : w.q0)) * a.Hq + w.h;
+                if (valid && stp.accumulate)
+                    prev2 = stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, qpos)] *
+                            1.4426950408889634f;
+            }
             // total row sum: this half's share plus the other's (exchange phase n;
             // buffer n&1 was last read before the phase n-1 arrivals)
             float *pmn = pm + (n & 1) * 256;
@@ -484,10 +549,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(BAR(B_MX));
             ok = waitw(BAR(B_MX), n & 1, wc);
             const float l_tot = pmn[row] + pmn[128 + row];
-            const bool valid = qpos < w.cend;
             const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const int qp = slot_pos(g, qpos);   // global position of the row
-            if constexpr (SPLIT) {
+            if constexpr (STEP) {
+                // merge the block (O / l, lse_blk) into the state (out_acc, lse):
+                // lse_new = ln(e^lse + e^lse_blk), out_new = e^(lse - lse_new) out_acc
+                // + e^(lse_blk - lse_new) O / l, in base 2; an empty side has
+                // weight 0, both empty leave (0, -inf)
+                const float blk2 = l_tot > 0.f ? m_run + lg2(l_tot) : NEG_INF;
+                const float mx = fmaxf(prev2, blk2);
+                float wa = 0.f, wb = 0.f, new2 = NEG_INF;
+                if (mx != NEG_INF) {
+                    const float ea = ex2(prev2 - mx), eb = ex2(blk2 - mx);   // ex2(-inf) = 0
+                    const float rs = 1.f / (ea + eb);
+                    new2 = mx + lg2(ea + eb);
+                    wa = ea * rs;
+                    wb = eb * rs * inv;
+                }
+                // a row that sees no key of this block keeps its state untouched
+                // (weights 1 and 0 give back its out exactly; its lse is not rewritten)
+                const bool keep = stp.accumulate && blk2 == NEG_INF;
+                if (keep) {
+                    wa = 1.f;
+                    wb = 0.f;
+                }
+                const bool write = valid;
+                float *orow = stp.out_acc + srow * D + (D / 2) * half;
+                __nv_bfloat16 *frow = static_cast<__nv_bfloat16 *>(stp.out_final) + srow * D + (D / 2) * half;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + 32u * c, o);
+                    if (write) {
+                        float4 *dst = reinterpret_cast<float4 *>(orow + 32 * c);
+                        uint4 *fdst = reinterpret_cast<uint4 *>(frow + 32 * c);
+                        // 8 columns at a time: two float4 of state, one uint4 of bf16
+#pragma unroll
+                        for (int v8 = 0; v8 < 4; ++v8) {
+                            float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+                            if (stp.accumulate) {
+                                p0 = dst[2 * v8];
+                                p1 = dst[2 * v8 + 1];
+                            }
+                            const uint32_t *ov = o + 8 * v8;
+                            const float4 r0 = make_float4(wa * p0.x + wb * __uint_as_float(ov[0]),
+                                                          wa * p0.y + wb * __uint_as_float(ov[1]),
+                                                          wa * p0.z + wb * __uint_as_float(ov[2]),
+                                                          wa * p0.w + wb * __uint_as_float(ov[3]));
+                            const float4 r1 = make_float4(wa * p1.x + wb * __uint_as_float(ov[4]),
+                                                          wa * p1.y + wb * __uint_as_float(ov[5]),
+                                                          wa * p1.z + wb * __uint_as_float(ov[6]),
+                                                          wa * p1.w + wb * __uint_as_float(ov[7]));
+                            dst[2 * v8] = r0;
+                            dst[2 * v8 + 1] = r1;
+                            if (stp.out_final)
+                                fdst[v8] = make_uint4(pack_bf16(r0.x, r0.y), pack_bf16(r0.z, r0.w),
+                                                      pack_bf16(r1.x, r1.y), pack_bf16(r1.z, r1.w));
+                        }
+                    }
+                }
+                if (ok && valid && !keep && half == 0)
+                    stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, qpos)] =
+                        new2 == NEG_INF ? NEG_INF : new2 * 0.69314718055994531f;
+            } else if constexpr (SPLIT) {
                 const int64_t prow = (((int64_t)sp * a.B + w.b) * a.S + qp) * a.Hq + w.h;
                 float *orow = so.out + prow * D + (D / 2) * half;
 #pragma unroll
@@ -538,33 +662,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // --- host side -----------------------------------------------------------------
 
-template <int D, bool SPLIT>
+template <int D, int MODE>
 int launch_d(const void *q, const void *k, const void *v, void *out, float *lse, FwdArgs a,
-             const SplitOut &so, cudaStream_t st)
+             const SplitOut &so, const StepOut &stp, cudaStream_t st)
 {
     CUtensorMap mq, mk, mv;
-    const int R = a.layout == CP_LAYOUT_STRIPED ? a.N : 1;
-    if (!make_map(&mq, q, a.B, a.S, a.Hq, D, 128, R) || !make_map(&mk, k, a.B, a.S, a.Hkv, D, KT, R) ||
-        !make_map(&mv, v, a.B, a.S, a.Hkv, D, 128, R))
-        return CP_ECUDA;
+    const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
+    if (MODE == MODE_STEP) {
+        // shard-local buffers: [B][S/N][H][D] in the shards' local row order
+        const int64_t C = (int64_t)g.clen * g.cpr;
+        if (!make_map(&mq, q, a.B, C, a.Hq, D, 128, 1) || !make_map(&mk, k, a.B, C, a.Hkv, D, KT, 1) ||
+            !make_map(&mv, v, a.B, C, a.Hkv, D, 128, 1))
+            return CP_ECUDA;
+    } else {
+        const int R = a.layout == CP_LAYOUT_STRIPED ? a.N : 1;
+        if (!make_map(&mq, q, a.B, a.S, a.Hq, D, 128, R) || !make_map(&mk, k, a.B, a.S, a.Hkv, D, KT, R) ||
+            !make_map(&mv, v, a.B, a.S, a.Hkv, D, 128, R))
+            return CP_ECUDA;
+    }
     static bool attr_done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CP_ECUDA;
     if (dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(fwd_bf16_kernel<D, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(fwd_bf16_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<D>::SMEM) != cudaSuccess)
             return CP_ECUDA;
         attr_done[dev] = true;
     }
-    const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
     a.upc = (g.clen + QT - 1) / QT;
     const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
     if (units == 0) return CP_OK;
-    const int64_t blocks = units * (SPLIT ? so.n : 1);
+    const int64_t blocks = units * (MODE == MODE_SPLIT ? so.n : 1);
     if (blocks > 0x7fffffffLL) return CP_EUNSUPPORTED;
     const float sl2 = a.scale * 1.4426950408889634f;
-    fwd_bf16_kernel<D, SPLIT><<<(unsigned)blocks, NTHREADS, Cfg<D>::SMEM, st>>>(
-        mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse, so);
+    fwd_bf16_kernel<D, MODE><<<(unsigned)blocks, NTHREADS, Cfg<D>::SMEM, st>>>(
+        mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse, so, stp);
     return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
 }
 
@@ -574,8 +706,9 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
                     FwdArgs a, cudaStream_t st)
 {
     const SplitOut none{1, nullptr, nullptr};
-    if (a.D == 64) return launch_d<64, false>(q, k, v, out, lse, a, none, st);
-    if (a.D == 128) return launch_d<128, false>(q, k, v, out, lse, a, none, st);
+    const StepOut nostep{0, 0, nullptr, nullptr, nullptr};
+    if (a.D == 64) return launch_d<64, MODE_RING>(q, k, v, out, lse, a, none, nostep, st);
+    if (a.D == 128) return launch_d<128, MODE_RING>(q, k, v, out, lse, a, none, nostep, st);
     return CP_EUNSUPPORTED;
 }
 
@@ -583,8 +716,19 @@ int launch_fwd_bf16_split(const void *q, const void *k, const void *v, FwdArgs a
                           const SplitOut &so, cudaStream_t st)
 {
     if (so.n < 1 || !so.out || !so.lse) return CP_EINVAL;
-    if (a.D == 64) return launch_d<64, true>(q, k, v, nullptr, nullptr, a, so, st);
-    if (a.D == 128) return launch_d<128, true>(q, k, v, nullptr, nullptr, a, so, st);
+    const StepOut nostep{0, 0, nullptr, nullptr, nullptr};
+    if (a.D == 64) return launch_d<64, MODE_SPLIT>(q, k, v, nullptr, nullptr, a, so, nostep, st);
+    if (a.D == 128) return launch_d<128, MODE_SPLIT>(q, k, v, nullptr, nullptr, a, so, nostep, st);
+    return CP_EUNSUPPORTED;
+}
+
+int launch_fwd_bf16_step(const void *q, const void *k, const void *v, FwdArgs a,
+                         const StepOut &stp, cudaStream_t st)
+{
+    if (!stp.out_acc || !stp.lse_acc || a.rank_hi != a.rank_lo + 1) return CP_EINVAL;
+    const SplitOut none{1, nullptr, nullptr};
+    if (a.D == 64) return launch_d<64, MODE_STEP>(q, k, v, nullptr, nullptr, a, none, stp, st);
+    if (a.D == 128) return launch_d<128, MODE_STEP>(q, k, v, nullptr, nullptr, a, none, stp, st);
     return CP_EUNSUPPORTED;
 }
 

@@ -12,6 +12,10 @@
 // 16-row query units and 32-key KV tiles, and folds every tile into the
 // running (O, m, l) with the online-softmax rescaling equations of
 // "Algorithmic Mechanics".
+//
+// STEP: one ring step of one rank on shard-local buffers (flash_block_step):
+// q is the rank's shard and k, v the source's block, in local row order; the
+// block's (out, lse) is merged into the running fp32 state in fp64.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -27,13 +31,13 @@ constexpr int TK = 32;      // keys per KV tile
 constexpr int WARPS = 8;
 constexpr int ROWS_PER_WARP = QR / WARPS;
 
-template <int D>
+template <int D, bool STEP>
 __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__restrict__ q,
                                                              const float *__restrict__ k,
                                                              const float *__restrict__ v,
                                                              float *__restrict__ out,
                                                              float *__restrict__ lse,
-                                                             FwdArgs a)
+                                                             FwdArgs a, const StepOut stp)
 {
     constexpr int DPL = D / 32;   // output elements per lane
     __shared__ float Qs[QR][D];
@@ -45,12 +49,15 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
     const int grp = a.Hq / a.Hkv;
     const int kvh = w.h / grp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C_loc = g.clen * g.cpr;   // rows of one shard (STEP buffers)
 
     // load the query rows of the unit (rows past the chunk end are zero)
     for (int i = threadIdx.x; i < QR * D; i += blockDim.x) {
         int rr = i / D, d = i % D;
         int pos = w.q0 + rr;   // slot; its global position is slot_pos
-        Qs[rr][d] = (pos < w.cend) ? q[(((int64_t)w.b * a.S + slot_pos(g, pos)) * a.Hq + w.h) * D + d] : 0.f;
+        const int64_t row = STEP ? (int64_t)w.b * C_loc + slot_lrow(g, w.r, pos)
+                                 : (int64_t)w.b * a.S + slot_pos(g, pos);
+        Qs[rr][d] = (pos < w.cend) ? q[(row * a.Hq + w.h) * D + d] : 0.f;
     }
 
     double o[ROWS_PER_WARP][DPL];
@@ -65,7 +72,10 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
     const double scale = (double)a.scale;
 
     KvIter<TK> it;
-    it.begin(g, w.r, w.qmax);
+    if (STEP)
+        it.begin_steps(g, w.r, w.qmax, stp.step_k, stp.step_k + 1);
+    else
+        it.begin(g, w.r, w.qmax);
     for (; it.valid(); it.next()) {
         const int ks = it.start();
         const int kl = it.len();
@@ -74,7 +84,9 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
             int j = i / D, d = i % D;
             float kv = 0.f, vv = 0.f;
             if (j < kl) {
-                int64_t off = (((int64_t)w.b * a.S + slot_pos(g, ks + j)) * a.Hkv + kvh) * D + d;
+                const int64_t row = STEP ? (int64_t)w.b * C_loc + it.lrow() + j
+                                         : (int64_t)w.b * a.S + slot_pos(g, ks + j);
+                int64_t off = (row * a.Hkv + kvh) * D + d;
                 kv = k[off];
                 vv = v[off];
             }
@@ -122,6 +134,34 @@ __global__ void __launch_bounds__(WARPS * 32) fwd_f32_kernel(const float *__rest
         const int qpos = w.q0 + rr;
         if (qpos >= w.cend) continue;
         const double inv = l[i] > 0.0 ? 1.0 / l[i] : 0.0;
+        if constexpr (STEP) {
+            // merge (o / l, m + ln l) into the state: lse_new = ln(e^lse + e^lse_blk),
+            // out_new = e^(lse - lse_new) out + e^(lse_blk - lse_new) o / l
+            const int64_t srow = ((int64_t)w.b * C_loc + slot_lrow(g, w.r, qpos)) * a.Hq + w.h;
+            float *lp = stp.lse_acc + ((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, qpos);
+            double prev = -INFINITY;
+            if (stp.accumulate) prev = __shfl_sync(0xffffffffu, lane == 0 ? (double)*lp : 0.0, 0);
+            const double blk = l[i] > 0.0 ? m[i] + log(l[i]) : -INFINITY;
+            const double mx = fmax(prev, blk);
+            double wa = 0.0, wb = 0.0, lnew = -INFINITY;
+            if (mx != -INFINITY) {
+                const double ea = exp(prev - mx), eb = exp(blk - mx);
+                lnew = mx + log(ea + eb);
+                wa = ea / (ea + eb);
+                wb = eb / (ea + eb) * inv;
+            }
+            float *orow = stp.out_acc + srow * D;
+            float *frow = static_cast<float *>(stp.out_final);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) {
+                const double pv = stp.accumulate ? (double)orow[lane + 32 * e] : 0.0;
+                const float r = (float)(wa * pv + wb * o[i][e]);
+                orow[lane + 32 * e] = r;
+                if (frow) frow[srow * D + lane + 32 * e] = r;
+            }
+            if (lane == 0) *lp = (float)lnew;
+            continue;
+        }
         const int qp = slot_pos(g, qpos);
         float *orow = out + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D;
 #pragma unroll
@@ -143,10 +183,28 @@ int launch_fwd_f32(const float *q, const float *k, const float *v, float *out, f
     if (units == 0) return CP_OK;
     if (units > 0x7fffffffLL) return CP_EUNSUPPORTED;
     dim3 grid((unsigned)units), block(WARPS * 32);
+    const StepOut nostep{0, 0, nullptr, nullptr, nullptr};
     if (a.D == 64)
-        fwd_f32_kernel<64><<<grid, block, 0, st>>>(q, k, v, out, lse, a);
+        fwd_f32_kernel<64, false><<<grid, block, 0, st>>>(q, k, v, out, lse, a, nostep);
     else
-        fwd_f32_kernel<128><<<grid, block, 0, st>>>(q, k, v, out, lse, a);
+        fwd_f32_kernel<128, false><<<grid, block, 0, st>>>(q, k, v, out, lse, a, nostep);
+    return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
+}
+
+int launch_fwd_f32_step(const float *q, const float *k, const float *v, FwdArgs a,
+                        const StepOut &stp, cudaStream_t st)
+{
+    if (!stp.out_acc || !stp.lse_acc || a.rank_hi != a.rank_lo + 1) return CP_EINVAL;
+    const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
+    a.upc = (g.clen + QR - 1) / QR;
+    const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
+    if (units == 0) return CP_OK;
+    if (units > 0x7fffffffLL) return CP_EUNSUPPORTED;
+    dim3 grid((unsigned)units), block(WARPS * 32);
+    if (a.D == 64)
+        fwd_f32_kernel<64, true><<<grid, block, 0, st>>>(q, k, v, nullptr, nullptr, a, stp);
+    else
+        fwd_f32_kernel<128, true><<<grid, block, 0, st>>>(q, k, v, nullptr, nullptr, a, stp);
     return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
 }
 

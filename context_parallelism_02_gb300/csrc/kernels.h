@@ -26,8 +26,24 @@ struct SplitOut {
     float *lse;
 };
 
+// State of a shard-local ring step (flash_block_step): the queries of rank
+// a.rank_lo (a.rank_hi = a.rank_lo + 1) in that rank's local row order,
+// against the KV block it holds at ring step step_k, merged into the running
+// (out_acc, lse_acc).  C = S / N rows per shard.
+struct StepOut {
+    int step_k;        // source rank = (rank - step_k) mod N
+    int accumulate;    // 0: the state is overwritten with this block's result
+    float *out_acc;    // [B][C][Hq][D] fp32, normalised output so far
+    float *lse_acc;    // [B][Hq][C] fp32, natural log
+    void *out_final;   // [B][C][Hq][D] in the input dtype (merged result), or null
+};
+
 int launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse,
                    FwdArgs a, cudaStream_t st);
+int launch_fwd_f32_step(const float *q, const float *k, const float *v, FwdArgs a,
+                        const StepOut &so, cudaStream_t st);
+int launch_fwd_bf16_step(const void *q, const void *k, const void *v, FwdArgs a,
+                         const StepOut &so, cudaStream_t st);
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse,
                     FwdArgs a, cudaStream_t st);
 int launch_fwd_bf16_split(const void *q, const void *k, const void *v, FwdArgs a,

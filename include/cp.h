@@ -128,6 +128,44 @@ int ring_attn_fwd_rank(const void *q, const void *k, const void *v, void *out, f
                        int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int layout,
                        int dtype, float scale, int rank_lo, int rank_hi, void *stream);
 
+/*
+ * flash_block_step -- one step of a real ring, on shard-local buffers: the
+ * flash_block(q, k, v, out, m, lse, source) call of the ring sketch in
+ * "Context Parallelism" ("Ring attention"), i.e. step k of "Algorithmic
+ * Mechanics" for one device.  The queries of `rank` attend to the KV block of
+ * `source` (the block held at ring step k = (rank - source) mod N), under the
+ * causal mask of the global positions of both shards ("Causal Masking and
+ * Load Balancing"), and the block's result is folded into the running state
+ * with the online-softmax rescaling written in log-sum-exp form:
+ *   lse_new = ln(e^lse_acc + e^lse_blk),
+ *   out_new = e^(lse_acc - lse_new) out_acc + e^(lse_blk - lse_new) out_blk.
+ * A ring runs N such steps per device, source = (rank - k) mod N for
+ * k = 0..N-1, while the KV block moves to rank + 1 (the caller's transfer).
+ * C = S / N is the shard length; every buffer is in the rank's (or the
+ * source's) local row order of cp_shard_map:
+ *   q [B][C][Hq][D]: the queries of `rank`; k, v [B][C][Hkv][D]: the block
+ *   of `source`; dtype CP_BF16 or CP_F32 (device).
+ *   out_acc [B][C][Hq][D] fp32 and lse_acc [B][Hq][C] fp32 (natural log):
+ *   the running normalised state, read and written (device).  accumulate = 0
+ *   overwrites it with this block's result (the first step; rows that see no
+ *   key of the block get out 0, lse -inf), accumulate = 1 merges into it.
+ *   The empty state (out 0, lse -inf) is the merge identity.
+ *   out_final: NULL, or [B][C][Hq][D] in the input dtype: the merged output
+ *   rounded to it (bf16: nearest even), e.g. on the last step.  For CP_F32 it
+ *   may alias out_acc.
+ *   S, N, layout, causal: the global sequence and its sharding (as for
+ *   ring_attn_fwd); rank, source in [0, N).  scale <= 0 selects 1/sqrt(D).
+ * Rows of the state that see no key of the block are left unchanged
+ * (accumulate = 1).  CP_BF16 runs the tcgen05 flash_block kernel (fp32
+ * accumulation); CP_F32 the precision path (fp64 arithmetic).
+ * Errors: as ring_attn_fwd, plus CP_EINVAL for rank, source or accumulate
+ * out of range and a misaligned out_final.
+ */
+int flash_block_step(const void *q, const void *k, const void *v, float *out_acc, float *lse_acc,
+                     void *out_final, int B, int Hq, int Hkv, int64_t S, int D, int N, int rank,
+                     int source, int causal, int layout, int dtype, float scale, int accumulate,
+                     void *stream);
+
 /* Largest n_split ring_attn_fwd_split accepts. */
 #define CP_MAX_SPLIT 64
 

@@ -62,6 +62,8 @@ def _load():
                                         i64, P, i64, i64, P, P]
             lib.or_ring_fwd.argtypes = [P, P, P, i32, i32, i32, i64, i32, i32, i32, i32,
                                         dbl, P, P]
+            lib.or_block_step.argtypes = [P, P, P, i32, i32, i32, i64, i32, i32, i32, i32,
+                                          i32, i32, dbl, i32, P, P]
             lib.or_lse_merge.argtypes = [P, P, P, P, i64, i32, P, P]
             lib.or_lse_merge_n.argtypes = [P, P, i32, i64, i32, P, P]
             lib.or_ulysses_seq_to_head.argtypes = [P, P, i32, i64, i32, i32, i32, i32, i32]
@@ -70,7 +72,7 @@ def _load():
                                         i64, P, i64, P, P, P, P]
             lib.or_num_threads.argtypes = []
             for f in ("or_shard_pos", "or_ring_source_table", "or_pair_counts", "or_attn_fwd",
-                      "or_ring_fwd", "or_lse_merge", "or_ulysses_seq_to_head",
+                      "or_ring_fwd", "or_block_step", "or_lse_merge", "or_ulysses_seq_to_head",
                       "or_ulysses_head_to_seq", "or_attn_bwd", "or_num_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -158,6 +160,30 @@ def ring_fwd(q, k, v, N: int, layout: int, causal: bool, scale: float | None = N
                              layout, float(scale), _ptr(out), _ptr(lse))
     _check(rc, "ring_fwd")
     return out, lse
+
+
+def block_step(q_shard, k_blk, v_blk, S: int, N: int, layout: int, causal: bool, rank: int,
+               source: int, out=None, lse=None, scale: float | None = None):
+    """One ring step of one device on shard-local buffers (fp64).
+
+    q_shard ``[B, C, Hq, D]`` holds rank ``rank``'s queries, k_blk / v_blk
+    ``[B, C, Hkv, D]`` rank ``source``'s keys and values, each in local order
+    (C = S / N).  ``out`` ``[B, C, Hq, D]`` / ``lse`` ``[B, Hq, C]`` is the
+    running state (None: start from the empty state).  Returns the new
+    (out, lse); the arguments are not modified.
+    """
+    q, k, v = _f64(q_shard), _f64(k_blk), _f64(v_blk)
+    B, C, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    acc = out is not None
+    o = _f64(out).copy() if acc else np.zeros((B, C, Hq, D))
+    l_ = _f64(lse).copy() if acc else np.zeros((B, Hq, C))
+    rc = _load().or_block_step(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, S, D, N, layout,
+                               int(causal), rank, source, float(scale), int(acc), _ptr(o), _ptr(l_))
+    _check(rc, "block_step")
+    return o, l_
 
 
 def lse_merge(out_a, lse_a, out_b, lse_b):

@@ -265,6 +265,83 @@ int or_ring_fwd(const double *q, const double *k, const double *v,
 }
 
 /* ------------------------------------------------------------------------ */
+/* One ring step of one device, on shard-local buffers (the flash_block call of
+ * the "Context Parallelism" ring sketch; one step k of "Algorithmic
+ * Mechanics").  q holds the C = S/N queries of rank r, k and v the C keys and
+ * values of rank src, each in that rank's local order (row t is global
+ * position or_pos(r, t)).  The state is the running normalised result:
+ * out [B][C][Hq][D], lse [B][Hq][C]; a normalised state is (O = out, m = lse,
+ * l = 1), or empty (l = 0) when lse = -inf.  The block statistics
+ * (m_block, l_block, unnormalised O_block) under the global-position causal
+ * mask are folded in with the same rescaling equations as or_ring_fwd.
+ * accumulate = 0 starts from the empty state. */
+int or_block_step(const double *q, const double *k, const double *v,
+                  int B, int Hq, int Hkv, int64_t S, int D, int N, int layout, int causal,
+                  int r, int src, double scale, int accumulate, double *out, double *lse)
+{
+    if (!or_layout_ok(S, N, layout) || Hkv < 1 || Hq % Hkv) return -1;
+    if (r < 0 || r >= N || src < 0 || src >= N) return -1;
+    const int grp = Hq / Hkv;
+    const int64_t C = S / N;
+    int64_t total = (int64_t)B * Hq * C;
+#pragma omp parallel
+    {
+        double *sblk = (double *)malloc(sizeof(double) * (size_t)(C > 0 ? C : 1));
+        double *ob = (double *)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t idx = 0; idx < total; ++idx) {
+            int64_t t = idx % C;
+            int h = (int)((idx / C) % Hq);
+            int b = (int)(idx / (C * Hq));
+            int g = h / grp;
+            int64_t p = or_pos(S, N, layout, r, t);
+            const double *qi = q + (((int64_t)b * C + t) * Hq + h) * D;
+            double *oi = out + (((int64_t)b * C + t) * Hq + h) * D;
+            double *li = lse + ((int64_t)b * Hq + h) * C + t;
+            /* the running state */
+            double m = accumulate ? *li : -INFINITY;
+            double l = (m == -INFINITY) ? 0.0 : 1.0;
+            if (!accumulate)
+                for (int d = 0; d < D; ++d) oi[d] = 0.0;
+            /* block statistics */
+            double mb = -INFINITY;
+            for (int64_t u = 0; u < C; ++u) {
+                int64_t j = or_pos(S, N, layout, src, u);
+                if (causal && j > p) { sblk[u] = -INFINITY; continue; }
+                const double *kj = k + (((int64_t)b * C + u) * Hkv + g) * D;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d) acc += qi[d] * kj[d];
+                sblk[u] = scale * acc;
+                if (sblk[u] > mb) mb = sblk[u];
+            }
+            if (mb == -INFINITY) {                      /* empty block: identity */
+                if (!accumulate) *li = -INFINITY;
+                continue;
+            }
+            double lb = 0.0;
+            for (int d = 0; d < D; ++d) ob[d] = 0.0;
+            for (int64_t u = 0; u < C; ++u) {
+                if (sblk[u] == -INFINITY) continue;
+                double e = exp(sblk[u] - mb);
+                lb += e;
+                const double *vj = v + (((int64_t)b * C + u) * Hkv + g) * D;
+                for (int d = 0; d < D; ++d) ob[d] += e * vj[d];
+            }
+            /* m_new, l_new, O_new as in or_ring_fwd */
+            double mn = m > mb ? m : mb;
+            double a = l * exp(m - mn);
+            double bb = exp(mb - mn);
+            double ln = a + lb * bb;
+            for (int d = 0; d < D; ++d) oi[d] = oi[d] * (a / ln) + ob[d] * (bb / ln);
+            *li = mn + log(ln);
+        }
+        free(sblk);
+        free(ob);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Merge of two normalised partial results (out_x, lse_x) over disjoint key
  * sets.  A normalised partial is the state (O = out_x, m = lse_x, l = 1), so
  * the rescaling equations give

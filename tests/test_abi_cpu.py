@@ -148,6 +148,23 @@ def test_argument_validation_without_gpu(cplib):
     assert split(lo=3, hi=3) == _lib.CP_EINVAL
     assert split(S=8200) == _lib.CP_EINVAL                            # zigzag: S % 2N
     assert split(B=0) == _lib.CP_OK                                   # empty batch
+    # flash_block_step: rank, source and accumulate are checked first
+    step = lambda **kw: L.flash_block_step(
+        *(kw.get(n, fake) for n in ("q", "k", "v", "oacc", "lacc")), kw.get("final", None),
+        kw.get("B", 1), 8, 8, kw.get("S", 8192), 128, kw.get("N", 8), kw.get("rank", 0),
+        kw.get("src", 7), 1, kw.get("layout", ZIG), kw.get("dtype", 1), -1.0, kw.get("acc", 1), None)
+    assert step(rank=8) == _lib.CP_EINVAL
+    assert step(rank=-1) == _lib.CP_EINVAL
+    assert step(src=8) == _lib.CP_EINVAL
+    assert step(acc=2) == _lib.CP_EINVAL
+    assert step(oacc=None) == _lib.CP_EINVAL
+    assert step(lacc=None) == _lib.CP_EINVAL
+    assert step(final=fake + 8) == _lib.CP_EINVAL                      # misaligned out_final
+    assert step(S=8200) == _lib.CP_EINVAL                             # zigzag: S % 2N
+    assert step(dtype=5) == _lib.CP_EUNSUPPORTED
+    assert step(B=0) == _lib.CP_OK                                    # empty batch
+    for code in (-6, -7):
+        assert _lib.strerror(code) != _lib.strerror(-99)
     buf = np.zeros(8, np.int32)
     assert L.cp_shard_map(12, 4, ZIG, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL
     assert L.cp_shard_map(1 << 40, 4, CONT, buf.ctypes.data_as(ctypes.c_void_p)) == _lib.CP_EINVAL

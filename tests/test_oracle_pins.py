@@ -43,6 +43,27 @@ def _sdpa(q, k, v, causal, scale=None):
     return o.permute(0, 2, 1, 3)
 
 
+def _shards(x, S, N, layout, pos_fn):
+    """Rank-local shards of a global-order [B, S, H, D] array (numpy), with the
+    local row order given by pos_fn(r) (global positions of rank r's rows)."""
+    return [np.ascontiguousarray(x[:, pos_fn(r)]) for r in range(N)]
+
+
+def _positions(S, N, layout):
+    """An independent restatement of the page's sharding (not the oracle's
+    mapper): contiguous blocks of S/N; zigzag chunks r and 2N-1-r of S/(2N);
+    striped positions r, r+N, r+2N, ..."""
+    def pos(r):
+        if layout == CONT:
+            return np.arange(r * (S // N), (r + 1) * (S // N))
+        if layout == STR:
+            return np.arange(r, S, N)
+        c = S // (2 * N)
+        return np.concatenate([np.arange(r * c, (r + 1) * c),
+                               np.arange((2 * N - 1 - r) * c, (2 * N - r) * c)])
+    return pos
+
+
 # ---------------------------------------------------------------- (a) brute force / library
 
 
@@ -477,3 +498,74 @@ def test_oracle_rejects_bad_shapes(oracle):
         oracle.shard_pos(12, 5, STR)
     with pytest.raises(ValueError):
         oracle.shard_pos(12, 4, 3)
+
+
+# ---------------------------------------------------------------- one ring step on local shards
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("layout", [CONT, ZIG, STR])
+@pytest.mark.parametrize("N", [1, 2, 3, 4])
+def test_block_steps_compose_to_attention(oracle, N, layout, causal):
+    """"What it does not change" / "Algorithmic Mechanics": the N ring steps of
+    one device, block of rank (r - k) mod N at step k, from the empty state,
+    give that device's rows of single-device attention (library SDPA)."""
+    S = 48 * N if layout != ZIG else 24 * 2 * N
+    q, k, v = _rand((2, S, 4, 8), 11), _rand((2, S, 2, 8), 12), _rand((2, S, 2, 8), 13)
+    ref = _sdpa(q, k, v, causal).numpy()
+    pos = _positions(S, N, layout)
+    qs, ks, vs = (_shards(x.numpy(), S, N, layout, pos) for x in (q, k, v))
+    for r in range(N):
+        out = lse = None
+        for step in range(N):
+            src = (r - step) % N
+            out, lse = oracle.block_step(qs[r], ks[src], vs[src], S, N, layout, causal, r, src,
+                                         out, lse)
+        np.testing.assert_allclose(out, ref[:, pos(r)], rtol=0, atol=1e-12)
+        assert np.isfinite(lse).all()
+
+
+def test_block_step_single_block_is_attention_over_its_keys(oracle):
+    """Contiguous shards: one step against source src equals definitional
+    attention restricted to src's key range (the oracle's O1 with a key range,
+    itself pinned to library attention); rows that see no key of the block
+    get the empty state (0, -inf)."""
+    S, N = 96, 4
+    C = S // N
+    q, k, v = _rand((1, S, 2, 8), 21), _rand((1, S, 2, 8), 22), _rand((1, S, 2, 8), 23)
+    for r in range(N):
+        for src in range(N):
+            out, lse = oracle.block_step(q[:, r * C:(r + 1) * C], k[:, src * C:(src + 1) * C],
+                                         v[:, src * C:(src + 1) * C], S, N, CONT, True, r, src)
+            rows = np.arange(r * C, (r + 1) * C)
+            ref, lref = oracle.attn_fwd(q, k, v, True, rows=rows, klo=src * C, khi=(src + 1) * C)
+            if src > r:   # every key of the block lies after every query
+                assert np.all(out == 0) and np.all(np.isneginf(lse))
+            else:
+                np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+                np.testing.assert_allclose(lse, lref, rtol=0, atol=1e-12)
+
+
+def test_block_step_order_free_and_empty_block_identity(oracle):
+    """The fold is the log-sum-exp merge, so the blocks can arrive in any order
+    (results equal to rounding); a block no query sees leaves the state
+    unchanged bit for bit."""
+    S, N, layout = 128, 4, ZIG
+    q, k, v = _rand((1, S, 2, 8), 31, 3.0), _rand((1, S, 2, 8), 32), _rand((1, S, 2, 8), 33)
+    pos = _positions(S, N, layout)
+    qs, ks, vs = (_shards(x.numpy(), S, N, layout, pos) for x in (q, k, v))
+    r = 2
+    res = []
+    for order in ([0, 1, 2, 3], [3, 1, 0, 2]):
+        out = lse = None
+        for src in order:
+            out, lse = oracle.block_step(qs[r], ks[src], vs[src], S, N, layout, True, r, src, out, lse)
+        res.append((out, lse))
+    np.testing.assert_allclose(res[0][0], res[1][0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(res[0][1], res[1][1], rtol=0, atol=1e-12)
+    # contiguous, causal: rank 0 sees nothing of rank 3's block
+    posc = _positions(S, N, CONT)
+    qc, kc, vc = (_shards(x.numpy(), S, N, CONT, posc) for x in (q, k, v))
+    out, lse = oracle.block_step(qc[0], kc[0], vc[0], S, N, CONT, True, 0, 0)
+    out2, lse2 = oracle.block_step(qc[0], kc[3], vc[3], S, N, CONT, True, 0, 3, out, lse)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
