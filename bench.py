@@ -8,11 +8,13 @@ TFLOP/s on masked-in FLOPs (4*D per visible (query, key) pair).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-With N > 1 (torchrun, one process per GPU) every rank runs its own replica of
-the workload (the path needs no collective on one device); the line reports
-the work of all ranks over the slowest rank's time.  ``--impl reference``
-times the fp64 CPU oracle on the host cores on a bounded sample of the same
-workload (rank 0 only).
+With N > 1 (torchrun, one process per GPU) the GPUs form a real ring: the
+same sequence is sharded over the N ranks (zigzag, 2N chunks), each rank runs
+N flash_block_step launches while the K/V blocks travel rank -> rank + 1 over
+NCCL point-to-point (ring.P2PTransport), and the line reports the whole
+sequence's masked-in FLOPs over the slowest rank's time ("scaling": "strong",
+the total work is fixed).  ``--impl reference`` times the fp64 CPU oracle on
+the host cores on a bounded sample of the same workload (rank 0 only).
 
 Prints one JSON line.
 """
@@ -376,6 +378,42 @@ def extras(dev, stream, peaks):
             "executed_tiles_128x256": int(tiles.sum()) * w.B * w.Hq,
         }
     out["per_rank_long128k"] = per
+    # the real ring's per-step launches: every (rank, step) of the long
+    # workload as flash_block_step on shard-local buffers (the launches one
+    # device of a 16-GPU ring makes), ranks run one after another; and the
+    # link rate at which a K/V hop would hide under one step's compute
+    from context_parallelism_02_gb300 import ring
+    lay = inputs.ZIGZAG
+    C = w.S // w.N
+    qs = [ring.shard(q, r, w.N, lay) for r in range(w.N)]
+    ks = [ring.shard(k, r, w.N, lay) for r in range(w.N)]
+    vs = [ring.shard(v, r, w.N, lay) for r in range(w.N)]
+    oacc = torch.empty(w.B, C, w.Hq, w.D, device=dev)
+    lacc = torch.empty(w.B, w.Hq, C, device=dev)
+    ofin = torch.empty_like(qs[0])
+
+    def ring_rank(r):
+        for s_ in range(w.N):
+            src = (r - s_) % w.N
+            api.flash_block_step(qs[r], ks[src], vs[src], r, src, w.N, w.S, lay, True,
+                                 out_acc=oacc, lse_acc=lacc,
+                                 out_final=ofin if s_ == w.N - 1 else None, accumulate=s_ > 0,
+                                 stream=stream)
+
+    rank_ms = []
+    for r in range(w.N):
+        ring_rank(r)
+        rank_ms.append(time_events(lambda: ring_rank(r), 3, stream))
+    hop = 2 * w.B * C * w.Hkv * w.D * 2
+    step_ms = sum(rank_ms) / len(rank_ms) / w.N
+    out["ring_steps_long128k"] = {
+        "ms_all_ranks_one_after_another": sum(rank_ms),
+        "ms_fused_ring_attn_fwd": per["zigzag"]["ms_all_ranks"],
+        "slowest_rank_ms": max(rank_ms), "rank_time_max_over_mean": max(rank_ms) / (sum(rank_ms) / len(rank_ms)),
+        "step_ms_mean": step_ms, "hop_bytes": hop,
+        "link_GBs_to_hide_hop": hop / (step_ms * 1e6),
+        "slowest_rank_TFLOPs": fwd_flops(w) / w.N / max(rank_ms) / 1e9}
+    del qs, ks, vs, oacc, lacc, ofin
     del q, k, v, ob, lb_
     # split-KV forward where it pays: one head of the long workload, one rank
     # per launch (64 query tiles of up to 512 KV tiles for 152 SMs), zigzag;
@@ -487,6 +525,148 @@ def hbm_summary(full, peaks):
     return out
 
 
+# ----------------------------------------------------------------------------- real ring (N > 1)
+
+def _timed(run, steps, warmup, world, device):
+    """ms per call of run() on this rank (CUDA events on the current stream, or
+    the host clock for CPU tensors), bracketed by a barrier and a device sync;
+    returns (max over ranks, this rank's)."""
+    import torch
+    import torch.distributed as dist
+    for _ in range(warmup):
+        run()
+    cuda = device.type == "cuda"
+    if cuda:
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if cuda:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run()
+    if cuda:
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+    else:
+        ms = (time.perf_counter() - t0) * 1e3 / steps
+    if world > 1:
+        dist.barrier()
+    return max_over_ranks(ms, world, device if cuda else "cpu"), ms
+
+
+def ring_measure(q, k, v, *, rank, world, S, layout, causal, steps, warmup, transport,
+                 blocks, step=None, state_dtype=None):
+    """Time one rank's part of a real ring three ways: the whole ring (compute
+    with the transfers overlapped), its N compute steps alone (the other
+    ranks' blocks taken from ``blocks``, as if already received), and its
+    N - 1 transfers alone.  q, k, v: this rank's shards; blocks[src] = (k, v)
+    of every rank.  Returns a dict of ms (max over ranks) and the fraction of
+    the transfer time hidden under compute."""
+    import torch
+    from context_parallelism_02_gb300 import ring
+    kw = dict(rank=rank, N=world, S=S, layout=layout, causal=causal)
+    step = step or ring.cuda_step
+    sdt = state_dtype or torch.float32
+    run_ring = lambda: ring.ring_attention(q, k, v, transport=transport, step=step,
+                                           state_dtype=sdt, **kw)
+    B, C, Hq, D = q.shape
+    oacc = torch.empty((B, C, Hq, D), dtype=sdt, device=q.device)
+    lacc = torch.empty((B, Hq, C), dtype=sdt, device=q.device)
+
+    def run_compute():
+        for s in range(world):
+            src = (rank - s) % world
+            step(q, blocks[src][0], blocks[src][1], oacc, lacc, None, source=src, scale=None,
+                 accumulate=s > 0, **kw)
+
+    bufs = [(torch.empty_like(k), torch.empty_like(v)) for _ in range(2)]
+
+    def run_comm():
+        cur = (k, v)
+        for s in range(world - 1):
+            h = transport.start(cur, bufs[s % 2])
+            transport.wait(h)
+            cur = bufs[s % 2]
+
+    dev = q.device
+    ms_ring, ms_ring_local = _timed(run_ring, steps, warmup, world, dev)
+    ms_comp, _ = _timed(run_compute, steps, warmup, world, dev)
+    ms_comm, _ = _timed(run_comm, steps, warmup, world, dev)
+    hidden = (ms_comp + ms_comm - ms_ring) / ms_comm if ms_comm > 0 else None
+    hop_bytes = 2 * k.numel() * k.element_size()
+    return {"ms_ring": ms_ring, "ms_ring_local": ms_ring_local, "ms_compute": ms_comp,
+            "ms_transfers": ms_comm, "transfer_hidden_frac": hidden, "hop_bytes": hop_bytes,
+            "hop_GBs": hop_bytes * (world - 1) / (ms_comm * 1e6) if ms_comm > 0 else None}
+
+
+def main_ring(args, w, world, rank, local, dev, stream, peaks):
+    """N > 1: the GPUs of the job form one ring over the workload's sequence."""
+    import torch
+    from context_parallelism_02_gb300 import api, inputs, ring
+    wl = w.with_(N=world)
+    q, k, v = inputs.make_qkv(wl)
+    pos_layout = wl.layout
+    qs, ks, vs = (ring.shard(x, rank, world, pos_layout).to(dev) for x in (q, k, v))
+    blocks = [tuple(ring.shard(x, r, world, pos_layout).to(dev) for x in (k, v)) for r in range(world)]
+    del q, k, v
+    transport = ring.P2PTransport()
+    sampler = ClockSampler(local)
+    sampler.start()
+    m = ring_measure(qs, ks, vs, rank=rank, world=world, S=wl.S, layout=wl.layout,
+                     causal=wl.causal, steps=args.steps, warmup=args.warmup,
+                     transport=transport, blocks=blocks)
+    clocks = sampler.stop()
+    assert api.cp_get_error() == 0
+    flops = fwd_flops(wl)
+    value = flops / (m["ms_ring"] * 1e-3) / 1e12
+    achieved_local = flops / world / (m["ms_compute"] * 1e-3) / 1e12
+    # end to end: this rank's shards uploaded from pinned host memory, the
+    # ring, and this rank's out and lse read back, every step
+    qh, kh, vh = (t.cpu().pin_memory() for t in (qs, ks, vs))
+    dq, dk, dv = (torch.empty_like(t) for t in (qs, ks, vs))
+    outs_h = {}
+
+    def e2e():
+        for d_, h_ in zip((dq, dk, dv), (qh, kh, vh)):
+            d_.copy_(h_, non_blocking=True)
+        o, l = ring.ring_attention(dq, dk, dv, rank=rank, N=world, S=wl.S, layout=wl.layout,
+                                   causal=wl.causal, transport=transport)
+        if not outs_h:
+            outs_h["o"] = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+            outs_h["l"] = torch.empty(l.shape, dtype=l.dtype, pin_memory=True)
+        outs_h["o"].copy_(o, non_blocking=True)
+        outs_h["l"].copy_(l, non_blocking=True)
+
+    e2e_ms, _ = _timed(e2e, max(3, min(args.steps, 10)), 2, world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = outs_h["o"].numel() * outs_h["o"].element_size() + outs_h["l"].numel() * 4
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_ring"],
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q, k, v drawn on the host)",
+        "config": {**config_of(wl, args.workload), "parallelism": f"ring over {world} GPUs (NCCL P2P)"},
+        "roofline": {"bound": "tensor", "achieved": achieved_local,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved_local / peaks["bf16_tflops"], "traffic": None,
+                     "kernel": "fwd_bf16_kernel<128, 2> (flash_block_step), per GPU",
+                     "note": "one GPU's masked-in FLOPs over its compute-only steps"},
+        "clocks": clocks,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "per rank: its shards uploaded from pinned memory, the ring, out and lse "
+                        "read back; h2d/d2h bytes are one rank's"},
+        "gpu_launches": args.steps * world,
+        "ring": rounded(m),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- ranks
 
 def max_over_ranks(x, world, device):
@@ -545,6 +725,10 @@ def main():
     # stream would order itself against the end-to-end copy streams)
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
+    if world > 1:
+        main_ring(args, w, world, rank, local, dev, stream, peaks)
+        dist.destroy_process_group()
+        return
 
     # inputs: drawn on the host (seeded), pinned, copied once to HBM
     qh, kh, vh = (t.pin_memory() for t in inputs.make_qkv(w))
@@ -647,11 +831,12 @@ def main():
     e2e_sampler = ClockSampler(local, getattr(torch.cuda.get_device_properties(dev), "uuid", None)
                                and "GPU-" + str(torch.cuda.get_device_properties(dev).uuid), 50)
     e2e_sampler.start()
-    # three repetitions of the pipelined steps, each with all its copies inside
-    # its own timed region; the median is reported (the host side of the box
-    # is shared, and one repetition can catch a stall there)
+    # five repetitions of the pipelined steps, each with all its copies inside
+    # its own timed region; the median is reported (the host link of these
+    # boxes drops for a while now and then from ~208 GB/s to ~15 GB/s, and a
+    # repetition that catches such a drop is copy-bound)
     e2e_all, fwd_only_all = [], []
-    for _ in range(3):
+    for _ in range(5):
         # the same forward with inputs already in HBM, timed right before the
         # end-to-end steps, so both see the same clocks and power state
         t0.record(stream)
@@ -679,15 +864,19 @@ def main():
     for name, st_, fn in (("h2d", up, lambda: upload(0)),
                           ("d2h", down, lambda: [h_.copy_(d_, non_blocking=True)
                                                  for h_, d_ in zip(outs_h[0], outs[0])])):
-        torch.cuda.synchronize()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(st_):
-            a0.record(st_)
-            fn()
-            a1.record(st_)
-        torch.cuda.synchronize()
-        link[name] = (h2d if name == "h2d" else d2h) / a0.elapsed_time(a1) / 1e6
+        rates = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(st_):
+                a0.record(st_)
+                fn()
+                a1.record(st_)
+            torch.cuda.synchronize()
+            rates.append((h2d if name == "h2d" else d2h) / a0.elapsed_time(a1) / 1e6)
+        link[name] = statistics.median(rates)
+        link[name + "_min"] = min(rates)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -701,7 +890,7 @@ def main():
                      "peak_source": f"{peak_src} bf16 dense ({peak_kind}; timed region "
                                     f"{args.steps * ms_local / 1e3:.2f} s)",
                      "frac_of_burst": achieved / peaks["bf16_tflops"],
-                     "kernel": "fwd_bf16_kernel<128, false>",
+                     "kernel": "fwd_bf16_kernel<128, 0> (ring mode)",
                      "flops_per_launch": flops},
         "clocks": clocks,
         "e2e": {"value": job_value(flops, world, e2e_ms), "unit": "TFLOP/s",
@@ -711,6 +900,7 @@ def main():
                 "e2e_over_fwd_only": e2e_ms / fwd_only_ms,
                 "rep_ms_min": min(e2e_all), "rep_ms_max": max(e2e_all),
                 "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"],
+                "link_h2d_gbs_min": link["h2d_min"], "link_d2h_gbs_min": link["d2h_min"],
                 "copy_ms_per_step": h2d / link["h2d"] / 1e6 + d2h / link["d2h"] / 1e6,
                 "sm_mhz": e2e_clocks.get("sm_mhz"),
                 "power_w_max": e2e_clocks.get("power_w_max"),

@@ -59,6 +59,7 @@ SIGNATURES = {
     "cp_get_error": (_I, [_P]),
     "cp_strerror": (ctypes.c_char_p, [_I]),
     "cp_debug_wait_timeout": (_I, [ctypes.c_uint64, _P]),
+    "cp_debug_set_wait_limit": (_I, [ctypes.c_uint64]),
 }
 
 _lock = threading.Lock()

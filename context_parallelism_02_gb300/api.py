@@ -336,6 +336,12 @@ def cp_strerror(code: int) -> str:
     return _lib.strerror(code)
 
 
+def cp_debug_set_wait_limit(limit_ns: int):
+    """Test hook: bound (ns) of the pipeline waits of later tensor-core launches
+    in this process; 0 restores the 2 s default (drains always keep 2 s)."""
+    check(_lib.load().cp_debug_set_wait_limit(int(limit_ns)), "cp_debug_set_wait_limit")
+
+
 def cp_debug_wait_timeout(limit_ns: int, stream=None):
     check(_lib.load().cp_debug_wait_timeout(limit_ns, ctypes.c_void_p(_stream(stream))),
           "cp_debug_wait_timeout")

@@ -200,7 +200,8 @@ struct BwdArgs {
     int upc;            // query units (128 rows) per chunk
     int tpc;            // key tiles per chunk
     unsigned *err;
-    uint64_t limit_ns;
+    uint64_t limit_ns;   // pipeline waits
+    uint64_t drain_ns;   // waits that drain copies and MMAs before exit
 };
 
 template <int D>
@@ -281,10 +282,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               it.mrank(), it.mrow(), w.b, pol_kv);
                 ++nk;
             }
-            if (*abort_flag) {
-                // wait (bounded) for the copies still in flight before the block exits
+            {
+                // wait (bounded) for the copies still in flight before the block
+                // exits: always, since a consumer may give up after the last copy
+                // was issued (after a normal run these phases are complete)
                 volatile int no_abort = 0;
-                WaitCtl dc{a.err, &no_abort, a.limit_ns};
+                WaitCtl dc{a.err, &no_abort, a.drain_ns};
                 for (int j = nk > Q_KST ? nk - Q_KST : 0; j < nk; ++j)
                     wait1(BAR(Q_KFULL + j % Q_KST), (j / Q_KST) & 1, dc);
             }
@@ -311,9 +314,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               it.mrank(), it.mrow(), w.b, pol_kv);
                 ++nv;
             }
-            if (*abort_flag) {
+            {
                 volatile int no_abort = 0;
-                WaitCtl dc{a.err, &no_abort, a.limit_ns};
+                WaitCtl dc{a.err, &no_abort, a.drain_ns};
                 wait1(BAR(Q_QTM), 0, dc);
                 wait1(BAR(Q_DOFULL), 0, dc);
                 for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) wait1(BAR(Q_VFULL + (j & 1)), (j >> 1) & 1, dc);
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             mma_commit(BAR(Q_DRAIN));
             volatile int no_abort = 0;
-            WaitCtl dc{a.err, &no_abort, a.limit_ns};
+            WaitCtl dc{a.err, &no_abort, a.drain_ns};
             wait1(BAR(Q_DRAIN), 0, dc);
         }
         __syncwarp();
@@ -650,10 +653,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 issued = s + 1;
                 if (hs) it.next();
             }
-            if (lane == 0 && *abort_flag) {
-                // wait (bounded) for the copies still in flight before the block exits
+            if (lane == 0) {
+                // wait (bounded) for the copies still in flight before the block
+                // exits: always, since a consumer may give up after the last copy
+                // was issued (after a normal run these phases are complete)
                 volatile int no_abort = 0;
-                WaitCtl dc{a.err, &no_abort, a.limit_ns};
+                WaitCtl dc{a.err, &no_abort, a.drain_ns};
                 wait1(BAR(K_KVFULL), 0, dc);
                 for (int s = issued > K_QST ? issued - K_QST : 0; s < issued; ++s)
                     wait1(BAR(K_QFULL + s % K_QST), (s / K_QST) & 1, dc);
@@ -707,7 +712,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             mma_commit(BAR(K_DRAIN));
             volatile int no_abort = 0;
-            WaitCtl dc{a.err, &no_abort, a.limit_ns};
+            WaitCtl dc{a.err, &no_abort, a.drain_ns};
             wait1(BAR(K_DRAIN), 0, dc);
         }
         __syncwarp();
@@ -909,6 +914,7 @@ int launch_bwd_bf16(const BwdPtrs &p, const FwdArgs &f, cudaStream_t st)
     a.upc = a.tpc = 0;
     a.err = f.err;
     a.limit_ns = f.limit_ns;
+    a.drain_ns = f.drain_ns;
     if (f.D == 64) return launch_bwd_d<64>(p, a, st);
     if (f.D == 128) return launch_bwd_d<128>(p, a, st);
     return CP_EUNSUPPORTED;

@@ -97,6 +97,7 @@ int noalloc_impl(const void *q, const void *k, const void *v, const void *out, c
     a.upc = 0;
     a.err = err;
     a.limit_ns = device_wait_limit_ns();
+    a.drain_ns = device_drain_limit_ns();
     BwdPtrs p{q, k, v, out, lse, dout, dq, dk, dv, scratch};
     return launch_bwd_bf16(p, a, static_cast<cudaStream_t>(stream));
 }

@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include <nvtx3/nvToolsExt.h>
@@ -22,6 +23,16 @@ namespace {
 
 constexpr int MAX_DEV = 64;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s per device-side wait
+
+// Bound of the pipeline waits of kernels launched from now on; 0 selects
+// WAIT_LIMIT_NS.  Only the cp_debug_set_wait_limit test hook changes it.
+std::atomic<uint64_t> g_pipeline_limit_ns{0};
+
+uint64_t pipeline_limit_ns()
+{
+    const uint64_t v = g_pipeline_limit_ns.load(std::memory_order_relaxed);
+    return v ? v : WAIT_LIMIT_NS;
+}
 
 unsigned *err_ptr()
 {
@@ -109,7 +120,8 @@ int prepare_fwd(const void *q, const void *k, const void *v, const void *out, co
     a.rank_hi = rank_hi;
     a.upc = 0;
     a.err = nullptr;
-    a.limit_ns = WAIT_LIMIT_NS;
+    a.limit_ns = pipeline_limit_ns();
+    a.drain_ns = WAIT_LIMIT_NS;
     return CP_OK;
 }
 
@@ -144,7 +156,9 @@ size_t split_workspace_bytes(int B, int Hq, int64_t S, int D, int n)
 
 unsigned *device_error_word() { return err_ptr(); }
 
-uint64_t device_wait_limit_ns() { return WAIT_LIMIT_NS; }
+uint64_t device_wait_limit_ns() { return pipeline_limit_ns(); }
+
+uint64_t device_drain_limit_ns() { return WAIT_LIMIT_NS; }
 
 int sm_count()
 {
@@ -352,7 +366,8 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
     a.rank_hi = N;
     a.upc = 0;
     a.err = err_ptr();
-    a.limit_ns = WAIT_LIMIT_NS;
+    a.limit_ns = pipeline_limit_ns();
+    a.drain_ns = WAIT_LIMIT_NS;
     if (!a.err) return CP_ECUDA;
     BwdPtrs p{q, k, v, out, lse, dout, dq, dk, dv, workspace};
     if (dtype == CP_F32) return launch_bwd_f32(p, a, static_cast<cudaStream_t>(stream));
@@ -503,6 +518,13 @@ const char *cp_strerror(int code)
         return "debug-bounds build: a kernel met an out-of-range tile coordinate and skipped it";
     default: return "unknown status code";
     }
+}
+
+int cp_debug_set_wait_limit(uint64_t limit_ns)
+{
+    if (limit_ns > WAIT_LIMIT_NS) return CP_EINVAL;
+    g_pipeline_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return CP_OK;
 }
 
 int cp_debug_wait_timeout(uint64_t limit_ns, void *stream)

@@ -474,6 +474,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the same phase (no suspension inside the instruction).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounds below this are the failure-path test hook's: the slow paths then poll
+// with the non-blocking test, so that a wait cannot be satisfied inside one
+// long suspension and the bound is what decides.
+constexpr uint64_t SHORT_WAIT_NS = 1000;
+
 // Shared state of the bounded waits of one block.
 struct WaitCtl {
     unsigned *err;          // device error word
@@ -493,10 +512,11 @@ __device__ __forceinline__ void raise_timeout(const WaitCtl &w)
 static __device__ __forceinline__ bool wait1_slow(uint32_t bar, uint32_t parity, WaitCtl w)
 {
     uint64_t t0 = globaltimer();
+    const bool poll = w.limit_ns < SHORT_WAIT_NS;
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*w.abort) return false;
         if (globaltimer() - t0 > w.limit_ns) {
             raise_timeout(w);
@@ -509,10 +529,12 @@ static __device__ __forceinline__ bool waitw_slow(uint32_t bar, uint32_t parity,
 {
     const unsigned FULL = 0xffffffffu;
     uint64_t t0 = globaltimer();
+    const bool poll = w.limit_ns < SHORT_WAIT_NS;
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+            if (__all_sync(FULL, poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)))
+                return true;
         int give_up = 0;
         if ((threadIdx.x & 31) == 0) {
             if (*w.abort) give_up = 1;

@@ -311,10 +311,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     nv = 2 * j + hh + 1;
                 }
             }
-            if (*abort_flag) {
-                // Drain: wait (bounded) for the copies still in flight.
+            {
+                // Drain: wait (bounded) for the copies still in flight -- always,
+                // since a consumer may give up after this thread has issued its last
+                // copy.  Each wait is on the last phase its barrier was armed for, so
+                // after a normal run every one of them is already complete.
                 volatile int no_abort = 0;
-                WaitCtl dc{a.err, &no_abort, a.limit_ns};
+                WaitCtl dc{a.err, &no_abort, a.drain_ns};
                 wait1(BAR(B_Q), 0, dc);
                 for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(B_KFULL + (j & 1)), (j >> 1) & 1, dc);
                 for (int x = nv > 2 ? nv - 2 : 0; x < nv; ++x) wait1(BAR(B_VFULL + (x & 1)), (x >> 1) & 1, dc);
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // arrivals: one commit per issuer) fires
             mma_commit(BAR(B_DRAIN));
             volatile int no_abort = 0;
-            WaitCtl dc{a.err, &no_abort, a.limit_ns};
+            WaitCtl dc{a.err, &no_abort, a.drain_ns};
             wait1(BAR(B_DRAIN), 0, dc);
         }
         // end of warpgroup 0: wait for every role, then warp 0 frees tensor memory

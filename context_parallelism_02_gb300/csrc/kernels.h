@@ -15,7 +15,8 @@ struct FwdArgs {
     int rank_lo, rank_hi; // virtual ranks whose queries are computed
     int upc;              // query units per chunk (set by the launcher)
     unsigned *err;        // device error word
-    uint64_t limit_ns;    // bound of every device-side wait
+    uint64_t limit_ns;    // bound of every pipeline wait
+    uint64_t drain_ns;    // bound of the waits that drain copies and MMAs before exit
 };
 
 // Partial results of a split forward (fp32, normalised): n splits of every
@@ -81,8 +82,10 @@ size_t bwd_workspace_bytes(int B, int Hq, int64_t S);
 int sm_count();
 
 // Device address of the current device's error word (set up once per device),
-// and the bound every device-side wait uses.
+// the bound of the pipeline waits (2 s unless a test shortened it with
+// cp_debug_set_wait_limit) and the bound of the drain waits (always 2 s).
 unsigned *device_error_word();
 uint64_t device_wait_limit_ns();
+uint64_t device_drain_limit_ns();
 
 }  // namespace cp

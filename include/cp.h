@@ -368,6 +368,19 @@ const char *cp_strerror(int code);
  */
 int cp_debug_wait_timeout(uint64_t limit_ns, void *stream);
 
+/*
+ * cp_debug_set_wait_limit -- test hook for the failure path of the pipelined
+ * tensor-core kernels (forward in every mode, the two backward kernels): the
+ * bound, in nanoseconds, of their pipeline waits for every launch made
+ * afterwards in this process; 0 restores the default (2 s).  The waits that
+ * drain a block's copies and MMAs before it exits keep the 2 s bound.  With
+ * a bound of a few nanoseconds the first wait that is not already satisfied
+ * runs out: the block records CP_ETIMEOUT, drains, frees its tensor memory
+ * and exits, and the context stays usable.  Process-wide; not for use while
+ * other threads launch work.  Errors: CP_EINVAL above 2e9.  Host only.
+ */
+int cp_debug_set_wait_limit(uint64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -103,3 +103,62 @@ def test_compact_line_fits_the_kept_output():
     assert text.index('"hbm_kernels"') > text.index('"extras"')
     assert line["hbm_kernels"]["lse_merge"]["frac_hbm"] == 0.9461
     assert line["extras"]["long128k_zigzag_rank_time_max_over_mean"] == 1.031
+
+
+def _ring_worker(rank, world, port, result):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        import oracle
+        from context_parallelism_02_gb300 import inputs, ring
+        w = inputs.Workload("bench_ring_cpu", 1, 2, 2, 64 * world, 16, world, 1, True,
+                            torch.float32, seed=7)
+        q, k, v = (t.double() for t in inputs.make_qkv(w))
+
+        def step(q_, k_, v_, out_acc, lse_acc, out_final, *, rank, source, N, S, layout, causal,
+                 scale, accumulate):
+            o, l_ = oracle.block_step(q_, k_, v_, S, N, layout, causal, rank, source,
+                                      out_acc if accumulate else None,
+                                      lse_acc if accumulate else None, scale)
+            out_acc.copy_(torch.from_numpy(o))
+            lse_acc.copy_(torch.from_numpy(l_))
+            if out_final is not None:
+                out_final.copy_(out_acc)
+
+        sh = lambda x, r: ring.shard(x, r, world, w.layout)
+        blocks = [(sh(k, r), sh(v, r)) for r in range(world)]
+        m = bench.ring_measure(sh(q, rank), sh(k, rank), sh(v, rank), rank=rank, world=world,
+                               S=w.S, layout=w.layout, causal=True, steps=2, warmup=1,
+                               transport=ring.P2PTransport(), blocks=blocks, step=step,
+                               state_dtype=torch.float64)
+        result[rank] = m
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_real_ring_measurement_on_gloo():
+    """bench.ring_measure's N > 1 logic (whole ring, compute alone, transfers
+    alone, max over ranks) with gloo ranks on CPU and the oracle's step."""
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    result = mgr.dict()
+    world, port = 2, _free_port()
+    procs = [ctx.Process(target=_ring_worker, args=(r, world, port, result)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(300)
+        assert p.exitcode == 0
+    for r in range(world):
+        m = result[r]
+        for key in ("ms_ring", "ms_compute", "ms_transfers"):
+            assert m[key] > 0
+        assert m["ms_ring"] == result[0]["ms_ring"]          # max over ranks
+        assert m["hop_bytes"] == 2 * 1 * 64 * 2 * 16 * 8     # k and v shards (C = 64), fp64
