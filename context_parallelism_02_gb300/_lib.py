@@ -5,6 +5,7 @@ The library must exist: there is no fallback path.  Build it with
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -62,8 +63,10 @@ SIGNATURES = {
     "cp_debug_set_wait_limit": (_I, [ctypes.c_uint64]),
 }
 
-_lock = threading.Lock()
-_lib = None
+_lock = threading.RLock()
+_libs = {}                 # variant -> loaded library
+_active = "default"        # the variant load() returns (see variant())
+_VARIANTS = {"default": (_build.LIB, {}), "debug_bounds": (_build.LIB_DEBUG_BOUNDS, {"debug_bounds": True})}
 
 
 class CpError(RuntimeError):
@@ -72,29 +75,45 @@ class CpError(RuntimeError):
         super().__init__(f"{what}: {strerror(code)} (code {code})")
 
 
-def lib_path() -> str:
-    return _build.LIB
+def lib_path(variant: str | None = None) -> str:
+    return _VARIANTS[variant or _active][0]
 
 
-def load(build_if_missing: bool = False):
-    """Load libcp.so (raises if it is missing: no fallback exists)."""
-    global _lib
+def load(build_if_missing: bool = False, variant: str | None = None):
+    """Load libcp.so (raises if it is missing: no fallback exists).  ``variant``
+    "debug_bounds" loads the checking build (default: the active variant)."""
+    v = variant or _active
     with _lock:
-        if _lib is None:
-            path = lib_path()
+        if v not in _libs:
+            path, opts = _VARIANTS[v]
             if not os.path.exists(path):
                 if not build_if_missing:
                     raise RuntimeError(
                         f"libcp.so not found at {path}; build it with "
                         "`python -m context_parallelism_02_gb300.build`")
-                _build.build()
+                _build.build(**opts)
             lib = ctypes.CDLL(path)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args
-            _lib = lib
-    return _lib
+            _libs[v] = lib
+    return _libs[v]
+
+
+@contextlib.contextmanager
+def variant(name: str):
+    """Route every binding call inside the block to the ``name`` build of libcp
+    (built if missing), e.g. ``with variant("debug_bounds"): ...``."""
+    global _active
+    with _lock:
+        prev = _active
+        load(build_if_missing=True, variant=name)
+        _active = name
+    try:
+        yield _libs[name]
+    finally:
+        _active = prev
 
 
 def strerror(code: int) -> str:

@@ -230,6 +230,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const Unit w = decode_unit_grouped(g, a.B, a.Hq, a.upc, T, blockIdx.x);
     const int kvh = w.h / (a.Hq / a.Hkv);
     const int n = KvIter<T>::count(g, w.r, w.qmax);
+    // extents of the tensor maps' (rank, row) dimensions, for the debug-bounds build
+    const int map_r = striped(g) ? g.N : 1, map_rows = a.S / map_r;
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(Q_QTM), 1);
@@ -277,9 +279,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int j = 0; j < n; ++j, it.next(), kr.next()) {
                 if (j >= Q_KST && !wait1(BAR(Q_KEMPTY + kr.st), kr.ph ^ 1, wc)) break;
                 mbar_arrive_expect_tx(BAR(Q_KFULL + kr.st), TB);
+                const int kmr = dbg_coord(a.err, it.mrank(), map_r), kmw = dbg_coord(a.err, it.mrow(), map_rows);
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load5(sK + kr.st * TB + bx * 16384, &tmK, BAR(Q_KFULL + kr.st), bx * 64, kvh,
-                              it.mrank(), it.mrow(), w.b, pol_kv);
+                              kmr, kmw, w.b, pol_kv);
                 ++nk;
             }
             {
@@ -294,14 +297,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         } else if (warp == 3 && lane == 0) {
             // ------------------------------------------------------------ dO and V producer
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+            const int qmr = dbg_coord(a.err, slot_mrank(g, w.q0), map_r);
+            const int qmw = dbg_coord(a.err, slot_mrow(g, w.q0), map_rows);
             mbar_arrive_expect_tx(BAR(Q_QTM), TB);
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load5(sQ + bx * 16384, &tmQ, BAR(Q_QTM), bx * 64, w.h, slot_mrank(g, w.q0),
-                          slot_mrow(g, w.q0), w.b, pol_q);
+                tma_load5(sQ + bx * 16384, &tmQ, BAR(Q_QTM), bx * 64, w.h, qmr, qmw, w.b, pol_q);
             mbar_arrive_expect_tx(BAR(Q_DOFULL), TB);
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load5(sDO + bx * 16384, &tmDO, BAR(Q_DOFULL), bx * 64, w.h, slot_mrank(g, w.q0),
-                          slot_mrow(g, w.q0), w.b, pol_q);
+                tma_load5(sDO + bx * 16384, &tmDO, BAR(Q_DOFULL), bx * 64, w.h, qmr, qmw, w.b, pol_q);
             KvIter<T> it;
             it.begin(g, w.r, w.qmax);
             int nv = 0;
@@ -309,9 +312,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int sv = j & 1;
                 if (j >= 2 && !wait1(BAR(Q_VEMPTY + sv), ((j >> 1) - 1) & 1, wc)) break;
                 mbar_arrive_expect_tx(BAR(Q_VFULL + sv), TB);
+                const int vmr = dbg_coord(a.err, it.mrank(), map_r), vmw = dbg_coord(a.err, it.mrow(), map_rows);
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load5(sV + sv * TB + bx * 16384, &tmV, BAR(Q_VFULL + sv), bx * 64, kvh,
-                              it.mrank(), it.mrow(), w.b, pol_kv);
+                              vmr, vmw, w.b, pol_kv);
                 ++nv;
             }
             {
@@ -391,8 +395,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tDQ = tmem + lane_off + C::TM_DQ;
         const uint32_t tDS = tmem + lane_off + C::TM_DS + 32u * half;
         const int qpos = w.q0 + row;                  // slot
-        const int qp = slot_pos(g, qpos);             // global position
         const bool valid = qpos < w.cend;
+        const int qp = dbg_coord(a.err, valid ? slot_pos(g, qpos) : 0, a.S);   // global position
         const float sl2 = a.scale * LOG2E;
         float lse2 = 0.f, dlt = 0.f;
         if (valid) {
@@ -572,6 +576,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
     const KvUnit w = decode_kv_unit<T>(g, a.B, a.Hkv, a.tpc, blockIdx.x);
     const int grp = a.Hq / a.Hkv;
+    // extents of the tensor maps' (rank, row) dimensions, for the debug-bounds build
+    const int map_r = striped(g) ? g.N : 1, map_rows = a.S / map_r;
     const int ns = 2 * QIter<T>::count(g, w.src, w.ks, grp);   // half steps
 
     if (threadIdx.x == 0) {
@@ -609,12 +615,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // ------------------------------------------------------------ producer (whole warp)
             const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
             if (lane == 0) {
+                const int kmr = dbg_coord(a.err, slot_mrank(g, w.ks), map_r);
+                const int kmw = dbg_coord(a.err, slot_mrow(g, w.ks), map_rows);
                 mbar_arrive_expect_tx(BAR(K_KVFULL), 2 * TB);
                 for (int bx = 0; bx < D / 64; ++bx) {
-                    tma_load5(sK + bx * 16384, &tmK, BAR(K_KVFULL), bx * 64, w.g, slot_mrank(g, w.ks),
-                              slot_mrow(g, w.ks), w.b, pol_kv);
-                    tma_load5(sV + bx * 16384, &tmV, BAR(K_KVFULL), bx * 64, w.g, slot_mrank(g, w.ks),
-                              slot_mrow(g, w.ks), w.b, pol_kv);
+                    tma_load5(sK + bx * 16384, &tmK, BAR(K_KVFULL), bx * 64, w.g, kmr, kmw, w.b, pol_kv);
+                    tma_load5(sV + bx * 16384, &tmV, BAR(K_KVFULL), bx * 64, w.g, kmr, kmw, w.b, pol_kv);
                 }
             }
             QIter<T> it;
@@ -625,13 +631,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (s >= K_QST && !waitw(BAR(K_QEMPTY + qr.st), qr.ph ^ 1, wc)) break;
                 const int hs = s & 1;
                 const int qa = it.start() + 64 * hs, ql = it.len() - 64 * hs, h = it.head();
-                const int qr_rank = it.mrank(), qr_row = it.mrow() + 64 * hs;   // map coordinates
+                // map coordinates; the second half-tile may start past the end of
+                // the map (a short last tile): the copy then reads the fill value
+                const int qr_rank = dbg_coord(a.err, it.mrank(), map_r);
+                const int qr_row = dbg_coord(a.err, it.mrow(), map_rows) + 64 * hs;
                 // per-row statistics of the half tile, negated: -lse (log2 units), -Delta
                 float *ls = stat + qr.st * 128, *dl = ls + 64;
                 for (int e = lane; e < 64; e += 32) {
                     float l2 = 0.f, dd = 0.f;
                     if (e < ql) {
-                        const int64_t off = ((int64_t)w.b * a.Hq + h) * a.S + slot_pos(g, qa + e);
+                        const int64_t off =
+                            ((int64_t)w.b * a.Hq + h) * a.S + dbg_coord(a.err, slot_pos(g, qa + e), a.S);
                         l2 = -lse[off] * LOG2E;
                         dd = -delta[off];
                     }
@@ -815,7 +825,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const bool valid = row < w.kl;
             const float f = half ? a.scale : 1.f;
             const uint32_t tAcc = tmem + lane_off + (half ? C::TM_DK : C::TM_DV);
-            __nv_bfloat16 *orow = (half ? dk : dv) + (((int64_t)w.b * a.S + slot_pos(g, kpos)) * a.Hkv + w.g) * D;
+            __nv_bfloat16 *orow =
+                (half ? dk : dv) + (((int64_t)w.b * a.S + dbg_coord(a.err, valid ? slot_pos(g, kpos) : 0, a.S)) * a.Hkv + w.g) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];

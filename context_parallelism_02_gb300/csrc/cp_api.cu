@@ -119,6 +119,7 @@ int prepare_fwd(const void *q, const void *k, const void *v, const void *out, co
     a.rank_lo = rank_lo;
     a.rank_hi = rank_hi;
     a.upc = 0;
+    a.head_grouped = 0;
     a.err = nullptr;
     a.limit_ns = pipeline_limit_ns();
     a.drain_ns = WAIT_LIMIT_NS;
@@ -365,6 +366,7 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
     a.rank_lo = 0;
     a.rank_hi = N;
     a.upc = 0;
+    a.head_grouped = 0;
     a.err = err_ptr();
     a.limit_ns = pipeline_limit_ns();
     a.drain_ns = WAIT_LIMIT_NS;

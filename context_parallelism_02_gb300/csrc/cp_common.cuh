@@ -493,6 +493,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 // long suspension and the bound is what decides.
 constexpr uint64_t SHORT_WAIT_NS = 1000;
 
+// Debug-bounds build (compiled with -DCP_DEBUG_BOUNDS): a tile coordinate or
+// row index outside [0, hi) is recorded in the error word (CP_EBOUNDS) and
+// replaced by 0, so the access itself stays in bounds; no trap.  In the
+// normal build this is the identity.
+__device__ __forceinline__ int dbg_coord(unsigned *err, int v, int hi)
+{
+#ifdef CP_DEBUG_BOUNDS
+    if (v < 0 || v >= hi) {
+        atomicCAS(err, 0u, ERRW_BOUNDS);
+        return 0;
+    }
+#else
+    (void)err;
+    (void)hi;
+#endif
+    return v;
+}
+
 // Shared state of the bounded waits of one block.
 struct WaitCtl {
     unsigned *err;          // device error word

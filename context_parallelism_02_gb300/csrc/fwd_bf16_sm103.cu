@@ -178,13 +178,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nunits = SPLIT ? (int)(gridDim.x / (unsigned)so.n) : (int)gridDim.x;
     const int sp = SPLIT ? (int)blockIdx.x / nunits : 0;
     const int ublk = SPLIT ? (int)blockIdx.x - sp * nunits : (int)blockIdx.x;
-    const Unit w = (a.rank_lo == 0 && a.rank_hi == a.N)
-                       ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, ublk)
+    const Unit w = a.head_grouped ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, ublk)
                        : decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, ublk);
     const int kvh = w.h / (a.Hq / a.Hkv);
     const int n_all = STEP ? KvIter<KT>::count(g, w.r, w.qmax, stp.step_k, stp.step_k + 1)
                            : KvIter<KT>::count(g, w.r, w.qmax);
     const int C_loc = g.clen * g.cpr;   // rows of one shard (MODE_STEP buffers)
+    // extents of the tensor maps' (rank, row) dimensions, for the debug-bounds build
+    const int map_r = (!STEP && striped(g)) ? g.N : 1;
+    const int map_rows = STEP ? C_loc : a.S / map_r;
     const int j0 = SPLIT ? (int)((int64_t)n_all * sp / so.n) : 0;
     const int n = SPLIT ? (int)((int64_t)n_all * (sp + 1) / so.n) - j0 : n_all;
     if (SPLIT && n == 0) {
@@ -267,10 +269,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
             mbar_arrive_expect_tx(BAR(B_Q), C::QBYTES);
             // map coordinates (rank, row) of the unit's first query
-            const int qmr = STEP ? 0 : slot_mrank(g, w.q0);
-            const int qmw = STEP ? slot_lrow(g, w.r, w.q0) : slot_mrow(g, w.q0);
+            const int qmr = dbg_coord(a.err, STEP ? 0 : slot_mrank(g, w.q0), map_r);
+            const int qmw = dbg_coord(a.err, STEP ? slot_lrow(g, w.r, w.q0) : slot_mrow(g, w.q0), map_rows);
+            const int qh = dbg_coord(a.err, w.h, a.Hq), qb = dbg_coord(a.err, w.b, a.B);
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, w.h, qmr, qmw, w.b, pol_q);
+                tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, qh, qmr, qmw, qb, pol_q);
             // K runs one tile ahead of V; the V loads reuse the K tile starts
             KvIter<KT> itk;
             if (STEP)
@@ -285,11 +288,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int st = j & 1;
                 if (j >= 2 && !wait1(BAR(B_KEMPTY + st), ((j >> 1) - 1) & 1, wc)) return false;
                 mbar_arrive_expect_tx(BAR(B_KFULL + st), C::KBYTES);
-                kr_next = STEP ? 0 : itk.mrank();
-                kw_next = STEP ? itk.lrow() : itk.mrow();
+                kr_next = dbg_coord(a.err, STEP ? 0 : itk.mrank(), map_r);
+                kw_next = dbg_coord(a.err, STEP ? itk.lrow() : itk.mrow(), map_rows);
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load5(sK + st * C::KBYTES + bx * C::KBOX, &tmK, BAR(B_KFULL + st), bx * 64,
-                              kvh, kr_next, kw_next, w.b, pol_kv);
+                              dbg_coord(a.err, kvh, a.Hkv), kr_next, kw_next, dbg_coord(a.err, w.b, a.B),
+                              pol_kv);
                 itk.next();
                 ++nk;
                 return true;
@@ -539,7 +543,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float prev2 = NEG_INF;
             int64_t srow = 0;
             if constexpr (STEP) {
-                srow = ((int64_t)w.b * C_loc + slot_lrow(g, w.r, valid ? qpos : w.q0)) * a.Hq + w.h;
+                srow = ((int64_t)w.b * C_loc + dbg_coord(a.err, slot_lrow(g, w.r, valid ? qpos : w.q0), C_loc)) *
+                           a.Hq + w.h;
                 if (valid && stp.accumulate)
                     prev2 = stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, qpos)] *
                             1.4426950408889634f;
@@ -615,7 +620,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, qpos)] =
                         new2 == NEG_INF ? NEG_INF : new2 * 0.69314718055994531f;
             } else if constexpr (SPLIT) {
-                const int64_t prow = (((int64_t)sp * a.B + w.b) * a.S + qp) * a.Hq + w.h;
+                const int64_t prow =
+                    (((int64_t)sp * a.B + w.b) * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h;
                 float *orow = so.out + prow * D + (D / 2) * half;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
@@ -632,7 +638,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (ok && valid && half == 0)
                     so.lse[prow] = l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
             } else {
-            __nv_bfloat16 *orow = out + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D + (D / 2) * half;
+            __nv_bfloat16 *orow =
+                out + (((int64_t)w.b * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h) * D + (D / 2) * half;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
@@ -693,6 +700,17 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
         attr_done[dev] = true;
     }
     a.upc = (g.clen + QT - 1) / QT;
+    // Unit order.  Blocks start in launch order on the SM that frees first, so
+    // numbering units longest first (heads fastest, descending position) is a
+    // longest-processing-time schedule.  But then the blocks in flight touch
+    // every head's K/V at once; when those exceed what L2 can keep
+    // (S = 131072: 512 MB), every query tile re-reads its K/V from DRAM, so a
+    // launch over all ranks numbers each (batch, head) contiguously instead
+    // (blocks in flight share one or two heads' K/V).  Below ~48 MB of K/V the
+    // longest-first order costs no DRAM traffic and shortens the tail.
+    const int64_t kv_bytes = 2ll * a.B * a.S * a.Hkv * D * 2;
+    a.head_grouped = (MODE != MODE_STEP && a.rank_lo == 0 && a.rank_hi == a.N &&
+                      kv_bytes > 48ll * 1024 * 1024) ? 1 : 0;
     const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
     if (units == 0) return CP_OK;
     const int64_t blocks = units * (MODE == MODE_SPLIT ? so.n : 1);

@@ -14,6 +14,7 @@ struct FwdArgs {
     float scale;          // softmax scale
     int rank_lo, rank_hi; // virtual ranks whose queries are computed
     int upc;              // query units per chunk (set by the launcher)
+    int head_grouped;     // units numbered with each (batch, head) contiguous (set by the launcher)
     unsigned *err;        // device error word
     uint64_t limit_ns;    // bound of every pipeline wait
     uint64_t drain_ns;    // bound of the waits that drain copies and MMAs before exit

@@ -30,6 +30,17 @@ def test_exports_every_declared_symbol(cplib):
     assert set(names) == set(_lib.SIGNATURES)
 
 
+def test_debug_bounds_variant_builds_and_exports(cplib):
+    """The -DCP_DEBUG_BOUNDS build compiles and exports the same entry points."""
+    from context_parallelism_02_gb300 import build
+    path = build.build(debug_bounds=True)
+    assert path != _lib.lib_path("default")
+    lib = _lib.load(variant="debug_bounds")
+    for n in _declared_symbols():
+        assert hasattr(lib, n), n
+    assert lib.cp_strerror(-7) == _lib.load().cp_strerror(-7)
+
+
 def test_library_is_in_tree(cplib):
     assert os.path.realpath(_lib.lib_path()).startswith(os.path.realpath(ROOT))
 
