@@ -61,6 +61,7 @@ SIGNATURES = {
     "cp_strerror": (ctypes.c_char_p, [_I]),
     "cp_debug_wait_timeout": (_I, [ctypes.c_uint64, _P]),
     "cp_debug_set_wait_limit": (_I, [ctypes.c_uint64]),
+    "cp_debug_set_grid_limit": (_I, [_I]),
 }
 
 _lock = threading.RLock()

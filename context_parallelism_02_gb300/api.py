@@ -342,6 +342,12 @@ def cp_debug_set_wait_limit(limit_ns: int):
     check(_lib.load().cp_debug_set_wait_limit(int(limit_ns)), "cp_debug_set_wait_limit")
 
 
+def cp_debug_set_grid_limit(max_blocks: int):
+    """Test hook: the tensor-core forward launches at most ``max_blocks`` blocks
+    (each running several work items); 0 restores the default grid."""
+    check(_lib.load().cp_debug_set_grid_limit(int(max_blocks)), "cp_debug_set_grid_limit")
+
+
 def cp_debug_wait_timeout(limit_ns: int, stream=None):
     check(_lib.load().cp_debug_wait_timeout(limit_ns, ctypes.c_void_p(_stream(stream))),
           "cp_debug_wait_timeout")

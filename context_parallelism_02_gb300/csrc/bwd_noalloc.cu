@@ -96,6 +96,7 @@ int noalloc_impl(const void *q, const void *k, const void *v, const void *out, c
     a.rank_hi = N;
     a.upc = 0;
     a.head_grouped = 0;
+    a.n_units = 0;
     a.err = err;
     a.limit_ns = device_wait_limit_ns();
     a.drain_ns = device_drain_limit_ns();

@@ -28,6 +28,10 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s per device-side wait
 // WAIT_LIMIT_NS.  Only the cp_debug_set_wait_limit test hook changes it.
 std::atomic<uint64_t> g_pipeline_limit_ns{0};
 
+// Largest grid of the forward kernel; 0: no limit.  Only the
+// cp_debug_set_grid_limit test hook changes it.
+std::atomic<int> g_fwd_grid_limit{0};
+
 uint64_t pipeline_limit_ns()
 {
     const uint64_t v = g_pipeline_limit_ns.load(std::memory_order_relaxed);
@@ -120,6 +124,7 @@ int prepare_fwd(const void *q, const void *k, const void *v, const void *out, co
     a.rank_hi = rank_hi;
     a.upc = 0;
     a.head_grouped = 0;
+    a.n_units = 0;
     a.err = nullptr;
     a.limit_ns = pipeline_limit_ns();
     a.drain_ns = WAIT_LIMIT_NS;
@@ -160,6 +165,8 @@ unsigned *device_error_word() { return err_ptr(); }
 uint64_t device_wait_limit_ns() { return pipeline_limit_ns(); }
 
 uint64_t device_drain_limit_ns() { return WAIT_LIMIT_NS; }
+
+int fwd_grid_limit() { return g_fwd_grid_limit.load(std::memory_order_relaxed); }
 
 int sm_count()
 {
@@ -367,6 +374,7 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
     a.rank_hi = N;
     a.upc = 0;
     a.head_grouped = 0;
+    a.n_units = 0;
     a.err = err_ptr();
     a.limit_ns = pipeline_limit_ns();
     a.drain_ns = WAIT_LIMIT_NS;
@@ -526,6 +534,13 @@ int cp_debug_set_wait_limit(uint64_t limit_ns)
 {
     if (limit_ns > WAIT_LIMIT_NS) return CP_EINVAL;
     g_pipeline_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return CP_OK;
+}
+
+int cp_debug_set_grid_limit(int max_blocks)
+{
+    if (max_blocks < 0) return CP_EINVAL;
+    g_fwd_grid_limit.store(max_blocks, std::memory_order_relaxed);
     return CP_OK;
 }
 

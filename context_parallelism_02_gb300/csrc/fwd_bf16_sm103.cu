@@ -77,7 +77,8 @@ enum {
     B_OFIN = 13,
     B_DRAIN = 14,
     B_MX = 15,       // one arrival per softmax warp (8): row maxima / sums published
-    NBAR = 16
+    B_QEMPTY = 16,   // a unit's S MMAs complete: the Q buffer may be reloaded
+    NBAR = 17
 };
 
 template <int D>
@@ -168,72 +169,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geom g = make_geom(a.S, a.N, a.layout, a.causal);
-    // a launch over every rank numbers its units with each (batch, head)
-    // contiguous: the blocks in flight then stream the K/V of one or two heads,
-    // which stay in L2; a launch over a subset of ranks keeps heads fastest
-    // split index slowest: the blocks in flight run the same split of
-    // consecutive units, which walk the same key tiles (as in an unsplit
-    // launch) and share them in L2; adjacent splits of one unit would walk
-    // disjoint key ranges and stream them from DRAM
-    const int nunits = SPLIT ? (int)(gridDim.x / (unsigned)so.n) : (int)gridDim.x;
-    const int sp = SPLIT ? (int)blockIdx.x / nunits : 0;
-    const int ublk = SPLIT ? (int)blockIdx.x - sp * nunits : (int)blockIdx.x;
-    const Unit w = a.head_grouped ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, ublk)
-                       : decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, ublk);
-    const int kvh = w.h / (a.Hq / a.Hkv);
-    const int n_all = STEP ? KvIter<KT>::count(g, w.r, w.qmax, stp.step_k, stp.step_k + 1)
-                           : KvIter<KT>::count(g, w.r, w.qmax);
     const int C_loc = g.clen * g.cpr;   // rows of one shard (MODE_STEP buffers)
     // extents of the tensor maps' (rank, row) dimensions, for the debug-bounds build
     const int map_r = (!STEP && striped(g)) ? g.N : 1;
     const int map_rows = STEP ? C_loc : a.S / map_r;
-    const int j0 = SPLIT ? (int)((int64_t)n_all * sp / so.n) : 0;
-    const int n = SPLIT ? (int)((int64_t)n_all * (sp + 1) / so.n) - j0 : n_all;
-    if (SPLIT && n == 0) {
-        // an empty split: the merge identity (out 0, lse -inf) for every row
-        const int rows = w.qmax - w.q0 + 1;
-        for (int i = threadIdx.x; i < rows * (D / 4); i += NTHREADS) {
-            const int rr = i / (D / 4), c4 = i - rr * (D / 4);
-            const int64_t orow = (((int64_t)sp * a.B + w.b) * a.S + slot_pos(g, w.q0 + rr)) * a.Hq + w.h;
-            reinterpret_cast<float4 *>(so.out + orow * D)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int rr = threadIdx.x; rr < rows; rr += NTHREADS)
-            so.lse[(((int64_t)sp * a.B + w.b) * a.S + slot_pos(g, w.q0 + rr)) * a.Hq + w.h] = -INFINITY;
-        return;
-    }
-    if (STEP && n == 0) {
-        // no key of this block is visible to the unit: merging changes nothing
-        // (out_final, if asked for, is the state rounded); a first step writes
-        // the empty state (out 0, lse -inf)
-        const int rows = w.qmax - w.q0 + 1;
-        if (stp.accumulate) {
-            if (stp.out_final)
-                for (int i = threadIdx.x; i < rows * (D / 8); i += NTHREADS) {
-                    const int rr = i / (D / 8), c8 = i - rr * (D / 8);
-                    const int64_t orow = ((int64_t)w.b * C_loc + slot_lrow(g, w.r, w.q0 + rr)) * a.Hq + w.h;
-                    const float4 *src = reinterpret_cast<const float4 *>(stp.out_acc + orow * D) + 2 * c8;
-                    const float4 x0 = src[0], x1 = src[1];
-                    reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(stp.out_final) + orow * D)[c8] =
-                        make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
-                                   pack_bf16(x1.z, x1.w));
-                }
-            return;
-        }
-        for (int i = threadIdx.x; i < rows * (D / 4); i += NTHREADS) {
-            const int rr = i / (D / 4), c4 = i - rr * (D / 4);
-            const int64_t orow = ((int64_t)w.b * C_loc + slot_lrow(g, w.r, w.q0 + rr)) * a.Hq + w.h;
-            reinterpret_cast<float4 *>(stp.out_acc + orow * D)[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (stp.out_final && c4 < D / 8)
-                reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(stp.out_final) + orow * D)[c4] =
-                    make_uint4(0u, 0u, 0u, 0u);
-        }
-        for (int rr = threadIdx.x; rr < rows; rr += NTHREADS)
-            stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, w.q0 + rr)] = -INFINITY;
-        return;
-    }
+    // Work items: the launch's units (times the splits).  Split index slowest:
+    // the blocks in flight run the same split of consecutive units, which walk
+    // the same key tiles (as in an unsplit launch) and share them in L2;
+    // adjacent splits of one unit would walk disjoint key ranges and stream
+    // them from DRAM.
+    const int nunits = a.n_units;
+    const int n_items = nunits * (SPLIT ? so.n : 1);
+
+    // The block runs items item_of(0), item_of(1), ...: rounds of gridDim.x
+    // items, alternately forwards and backwards over the longest-first
+    // numbering, so the blocks' totals stay close.  With one block per item
+    // (gridDim.x == n_items) the block runs item blockIdx.x alone.
+    auto item_of = [&](int it) -> int {
+        const int64_t G = gridDim.x, c = blockIdx.x;
+        const int64_t item = it * G + ((it & 1) ? G - 1 - c : c);
+        return item < n_items ? (int)item : n_items;
+    };
+    struct Item {
+        Unit w;
+        int sp, j0, n, kvh;
+    };
+    auto decode = [&](int item) -> Item {
+        Item x;
+        x.sp = SPLIT ? item / nunits : 0;
+        const int ublk = SPLIT ? item - x.sp * nunits : item;
+        x.w = a.head_grouped ? decode_unit_grouped(g, a.B, a.Hq, a.upc, QT, ublk)
+                             : decode_unit(g, a.B, a.Hq, a.rank_lo, a.rank_hi, a.upc, QT, ublk);
+        x.kvh = x.w.h / (a.Hq / a.Hkv);
+        const int n_all = STEP ? KvIter<KT>::count(g, x.w.r, x.w.qmax, stp.step_k, stp.step_k + 1)
+                               : KvIter<KT>::count(g, x.w.r, x.w.qmax);
+        x.j0 = SPLIT ? (int)((int64_t)n_all * x.sp / so.n) : 0;
+        x.n = SPLIT ? (int)((int64_t)n_all * (x.sp + 1) / so.n) - x.j0 : n_all;
+        return x;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_Q), 1);
+        mbar_init(BAR(B_QEMPTY), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(B_KFULL + i), 1);
             mbar_init(BAR(B_KEMPTY + i), 1);
@@ -262,57 +239,73 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{a.err, abort_flag, a.limit_ns};
 
+    // Phases run on across the block's items: every barrier's phase index is a
+    // running count (Q loads, K/V tiles, S and PV tiles, units, exchanges).
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------------------ producer
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
-            mbar_arrive_expect_tx(BAR(B_Q), C::QBYTES);
-            // map coordinates (rank, row) of the unit's first query
-            const int qmr = dbg_coord(a.err, STEP ? 0 : slot_mrank(g, w.q0), map_r);
-            const int qmw = dbg_coord(a.err, STEP ? slot_lrow(g, w.r, w.q0) : slot_mrow(g, w.q0), map_rows);
-            const int qh = dbg_coord(a.err, w.h, a.Hq), qb = dbg_coord(a.err, w.b, a.B);
-            for (int bx = 0; bx < D / 64; ++bx)
-                tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, qh, qmr, qmw, qb, pol_q);
-            // K runs one tile ahead of V; the V loads reuse the K tile starts
-            KvIter<KT> itk;
-            if (STEP)
-                itk.begin_steps(g, w.r, w.qmax, stp.step_k, stp.step_k + 1);
-            else
-                itk.begin(g, w.r, w.qmax);
-            if (SPLIT) itk.skip(j0);
-            int nk = 0, nv = 0;   // tiles whose K / V loads were issued
-            int kr_cur = 0, kw_cur = 0, kr_next = 0, kw_next = 0;   // map coordinates (rank, row)
+            int nq = 0, nk = 0, nv = 0;   // Q loads, K tiles, V halves issued so far
             bool ok = true;
-            auto load_k = [&](int j) -> bool {
-                const int st = j & 1;
-                if (j >= 2 && !wait1(BAR(B_KEMPTY + st), ((j >> 1) - 1) & 1, wc)) return false;
-                mbar_arrive_expect_tx(BAR(B_KFULL + st), C::KBYTES);
-                kr_next = dbg_coord(a.err, STEP ? 0 : itk.mrank(), map_r);
-                kw_next = dbg_coord(a.err, STEP ? itk.lrow() : itk.mrow(), map_rows);
+            for (int it = 0; ok; ++it) {
+                const int item = item_of(it);
+                if (item >= n_items) break;
+                const Item x = decode(item);
+                if (x.n == 0) continue;
+                // the previous unit's S MMAs must be done with the single Q buffer
+                if (nq > 0 && !wait1(BAR(B_QEMPTY), (nq - 1) & 1, wc)) break;
+                mbar_arrive_expect_tx(BAR(B_Q), C::QBYTES);
+                // map coordinates (rank, row) of the unit's first query
+                const int qmr = dbg_coord(a.err, STEP ? 0 : slot_mrank(g, x.w.q0), map_r);
+                const int qmw = dbg_coord(a.err, STEP ? slot_lrow(g, x.w.r, x.w.q0) : slot_mrow(g, x.w.q0), map_rows);
+                const int qh = dbg_coord(a.err, x.w.h, a.Hq), qb = dbg_coord(a.err, x.w.b, a.B);
                 for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load5(sK + st * C::KBYTES + bx * C::KBOX, &tmK, BAR(B_KFULL + st), bx * 64,
-                              dbg_coord(a.err, kvh, a.Hkv), kr_next, kw_next, dbg_coord(a.err, w.b, a.B),
-                              pol_kv);
-                itk.next();
-                ++nk;
-                return true;
-            };
-            if (n > 0) ok = load_k(0);
-            for (int j = 0; ok && j < n; ++j) {
-                kr_cur = kr_next;
-                kw_cur = kw_next;
-                if (j + 1 < n && !load_k(j + 1)) break;
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (j >= 1 && !wait1(BAR(B_VEMPTY + hh), (j - 1) & 1, wc)) {
+                    tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, qh, qmr, qmw, qb, pol_q);
+                ++nq;
+                // K runs one tile ahead of V; the V loads reuse the K tile starts
+                KvIter<KT> itk;
+                if (STEP)
+                    itk.begin_steps(g, x.w.r, x.w.qmax, stp.step_k, stp.step_k + 1);
+                else
+                    itk.begin(g, x.w.r, x.w.qmax);
+                if (SPLIT) itk.skip(x.j0);
+                int kr_cur = 0, kw_cur = 0, kr_next = 0, kw_next = 0;   // map coordinates (rank, row)
+                const int kvh = dbg_coord(a.err, x.kvh, a.Hkv);
+                auto load_k = [&]() -> bool {   // the next K tile, global index nk
+                    const int st = nk & 1;
+                    if (nk >= 2 && !wait1(BAR(B_KEMPTY + st), ((nk >> 1) - 1) & 1, wc)) return false;
+                    mbar_arrive_expect_tx(BAR(B_KFULL + st), C::KBYTES);
+                    kr_next = dbg_coord(a.err, STEP ? 0 : itk.mrank(), map_r);
+                    kw_next = dbg_coord(a.err, STEP ? itk.lrow() : itk.mrow(), map_rows);
+                    for (int bx = 0; bx < D / 64; ++bx)
+                        tma_load5(sK + st * C::KBYTES + bx * C::KBOX, &tmK, BAR(B_KFULL + st), bx * 64,
+                                  kvh, kr_next, kw_next, qb, pol_kv);
+                    itk.next();
+                    ++nk;
+                    return true;
+                };
+                ok = load_k();
+                for (int j = 0; ok && j < x.n; ++j) {
+                    kr_cur = kr_next;
+                    kw_cur = kw_next;
+                    // global index of tile j: nv / 2 (V halves are issued tile by tile)
+                    const int t = nv >> 1;
+                    if (j + 1 < x.n && !load_k()) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(BAR(B_VFULL + hh), C::VBYTES);
-                    for (int bx = 0; bx < D / 64; ++bx)
-                        tma_load5(sV + hh * C::VBYTES + bx * 16384, &tmV, BAR(B_VFULL + hh), bx * 64,
-                                  kvh, kr_cur, kw_cur + 128 * hh, w.b, pol_kv);
-                    nv = 2 * j + hh + 1;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (t >= 1 && !wait1(BAR(B_VEMPTY + hh), (t - 1) & 1, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(BAR(B_VFULL + hh), C::VBYTES);
+                        for (int bx = 0; bx < D / 64; ++bx)
+                            tma_load5(sV + hh * C::VBYTES + bx * 16384, &tmV, BAR(B_VFULL + hh), bx * 64,
+                                      kvh, kr_cur, kw_cur + 128 * hh, qb, pol_kv);
+                        ++nv;
+                    }
                 }
             }
             {
@@ -322,7 +315,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // after a normal run every one of them is already complete.
                 volatile int no_abort = 0;
                 WaitCtl dc{a.err, &no_abort, a.drain_ns};
-                wait1(BAR(B_Q), 0, dc);
+                if (nq > 0) wait1(BAR(B_Q), (nq - 1) & 1, dc);
                 for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(B_KFULL + (j & 1)), (j >> 1) & 1, dc);
                 for (int x = nv > 2 ? nv - 2 : 0; x < nv; ++x) wait1(BAR(B_VFULL + (x & 1)), (x >> 1) & 1, dc);
             }
@@ -337,40 +330,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t idS = idesc_bf16(128, KT, false);
             constexpr uint32_t idO = idesc_bf16(128, D, true);
             const uint32_t tS = tmem, tP = tmem + 256u, tO = tmem + 384u;
-            bool ok = n > 0;
+            bool ok = true;
+            int nq = 0, nt = 0;   // units started, tiles issued so far
             if (warp == 1) {
                 const uint64_t dQ = sdesc(sQ, 16, 1024);
                 const uint64_t dK0 = sdesc(sK, 16, 1024);
-                ok = ok && wait1(BAR(B_Q), 0, wc);
-                for (int j = 0; ok && j < n; ++j) {
-                    const int st = j & 1;
-                    if (j > 0 && !wait1(BAR(B_SFREE), (j - 1) & 1, wc)) break;
-                    if (!wait1(BAR(B_KFULL + st), (j >> 1) & 1, wc)) break;
-                    tc_fence_after();
-                    issue_s_seq<0, D>(tS, dQ, dK0 + (uint64_t)(st * (C::KBYTES >> 4)), idS);
-                    mma_commit(BAR(B_SFULL));
-                    mma_commit(BAR(B_KEMPTY + st));
-                }
-            } else {
-                const uint64_t dV0 = sdesc(sV, 16384, 1024);
-                for (int j = 0; ok && j < n; ++j) {
-                    if (!wait1(BAR(B_PFULL), j & 1, wc)) break;
-                    tc_fence_after();
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (!wait1(BAR(B_VFULL + hh), j & 1, wc)) {
+                for (int it = 0; ok; ++it) {
+                    const int item = item_of(it);
+                    if (item >= n_items) break;
+                    const int n = decode(item).n;
+                    if (n == 0) continue;
+                    if (!wait1(BAR(B_Q), nq & 1, wc)) break;
+                    for (int j = 0; j < n; ++j, ++nt) {
+                        const int st = nt & 1;
+                        if ((nt > 0 && !wait1(BAR(B_SFREE), (nt - 1) & 1, wc)) ||
+                            !wait1(BAR(B_KFULL + st), (nt >> 1) & 1, wc)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        if (hh == 0)
-                            issue_pv_seq<0, 0>(tO, tP, dV0, idO, j > 0 ? 1u : 0u);
-                        else
-                            issue_pv_seq<0, 1>(tO, tP, dV0 + (uint64_t)(C::VBYTES >> 4), idO, 1u);
-                        mma_commit(BAR(B_VEMPTY + hh));
+                        issue_s_seq<0, D>(tS, dQ, dK0 + (uint64_t)(st * (C::KBYTES >> 4)), idS);
+                        mma_commit(BAR(B_SFULL));
+                        mma_commit(BAR(B_KEMPTY + st));
                     }
                     if (!ok) break;
-                    mma_commit(BAR(B_PFREE));
-                    if (j + 1 == n) mma_commit(BAR(B_OFIN));
+                    // Q may be reloaded once the unit's S MMAs have completed
+                    mma_commit(BAR(B_QEMPTY));
+                    ++nq;
+                }
+            } else {
+                const uint64_t dV0 = sdesc(sV, 16384, 1024);
+                for (int it = 0; ok; ++it) {
+                    const int item = item_of(it);
+                    if (item >= n_items) break;
+                    const int n = decode(item).n;
+                    for (int j = 0; j < n; ++j, ++nt) {
+                        // P(nt) written: every softmax warp has also finished reading
+                        // the previous unit's O, which the first PV of this unit
+                        // (accumulate 0) overwrites
+                        if (!wait1(BAR(B_PFULL), nt & 1, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        for (int hh = 0; hh < 2; ++hh) {
+                            if (!wait1(BAR(B_VFULL + hh), nt & 1, wc)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            if (hh == 0)
+                                issue_pv_seq<0, 0>(tO, tP, dV0, idO, j > 0 ? 1u : 0u);
+                            else
+                                issue_pv_seq<0, 1>(tO, tP, dV0 + (uint64_t)(C::VBYTES >> 4), idO, 1u);
+                            mma_commit(BAR(B_VEMPTY + hh));
+                        }
+                        if (!ok) break;
+                        mma_commit(BAR(B_PFREE));
+                        if (j + 1 == n) mma_commit(BAR(B_OFIN));
+                    }
                 }
             }
             // all MMAs of this thread are complete once the drain barrier (two
@@ -399,145 +417,198 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tS = tmem + lane_off + 128u * half;
         const uint32_t tP = tmem + lane_off + 256u + 64u * half;
         const uint32_t tO = tmem + lane_off + 384u + (uint32_t)(D / 2) * half;
-        const int qpos = w.q0 + row;
         const float NEG_INF = -INFINITY;
-        float m_run = NEG_INF, l_run = 0.f;      // l_run: this half's share of the row sum
         bool ok = true;
+        int nu = 0, nt = 0, nx = 0;   // units finished, tiles done, row-max exchanges so far
 
-        KvIter<KT> it;
-        if (STEP)
-            it.begin_steps(g, w.r, w.qmax, stp.step_k, stp.step_k + 1);
-        else
-            it.begin(g, w.r, w.qmax);
-        if (SPLIT) it.skip(j0);
-        for (int j = 0; j < n; ++j, it.next()) {
-            if (!waitw(BAR(B_SFULL), j & 1, wc)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sr[128];
-            tmem_ld_x128(tS, sr);
-            // S(j) may now be overwritten: one arrival per warp (per-thread
-            // arrivals would serialise 256 atomics on one shared-memory word)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_SFREE));
-            float *s = reinterpret_cast<float *>(sr);
-            const int ks = it.start();
-            const int kl = it.len();
-            if (kl < KT || (a.causal && ks + kl - 1 > w.q0 + it.shift)) {
-                // partial tile: key columns [0, lim) of the 256 are visible to this row
-                int lim = kl;
-                if (a.causal) {
-                    const int c = qpos - ks + 1 + it.shift;
-                    lim = c < lim ? c : lim;
-                }
-                lim -= 128 * half;
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c >= lim) s[c] = NEG_INF;
-            }
-            // row max over this half: four independent 3-input max chains
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-            for (int c = 4; c < 124; c += 8) {
-                mx0 = fmax3(mx0, s[c], s[c + 1]);
-                mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-                mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-                mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
-            }
-            mx0 = fmax3(mx0, s[124], s[125]);
-            mx1 = fmax3(mx1, s[126], s[127]);
-            mx0 = fmax3(mx0, mx2, mx3);
-            // Publish this half's row maximum (double-buffered by tile parity; the
-            // barrier's phase j completes once all 256 threads published theirs).
-            float *pmj = pm + (j & 1) * 256;
-            const float mloc = fmaxf(mx0, mx1) * sl2;
-            pmj[half * 128 + row] = fmaxf(mx0, mx1);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_MX));
-            // The exponentials use the running max m_run as long as this half's own
-            // maximum stays within 2^8 of it (P <= 2^8, no overflow), so the exchange
-            // is off the critical path; the combined max is checked afterwards and,
-            // in the rare case it grew by more than 2^8, P is scaled down to the new
-            // max.  The first visible tile (m_run = -inf) and a half whose own max
-            // jumped take the exchanged max first.
-            const bool early = __any_sync(0xffffffffu, mloc > m_run + RESCALE_LOG2);
-            float mt = NEG_INF;
-            if (early) {
-                if (!waitw(BAR(B_MX), j & 1, wc)) {
-                    ok = false;
-                    break;
-                }
-                mt = fmaxf(pmj[0 * 128 + row], pmj[1 * 128 + row]) * sl2;
-            }
-            float mn = fmaxf(m_run, mt);
-            bool need = mn > m_run + RESCALE_LOG2;
-            float f = need ? ex2(m_run - mn) : 1.f;    // ex2(-inf) = 0 on the first tile
-            if (need) m_run = mn;
-            const float mu = (m_run == NEG_INF) ? 0.f : m_run;
-            // P = exp2(s*sl2 - mu), packed to bf16 as it is produced
-            float l0 = 0.f, l1 = 0.f;
-            uint32_t pk0[32], pk1[32];
-#pragma unroll
-            for (int c = 0; c < 128; c += 2) {
-                float x0, x1;
-                ffma2(x0, x1, s[c], s[c + 1], sl2, -mu);
-                const float p0 = ex2(x0), p1 = ex2(x1);
-                const uint32_t pk = pack_bf16(p0, p1);
-                fadd2(l0, l1, p0, p1);
-                if (c < 64) pk0[c / 2] = pk;
-                else pk1[(c - 64) / 2] = pk;
-            }
-            if (!early) {
-                if (!waitw(BAR(B_MX), j & 1, wc)) {
-                    ok = false;
-                    break;
-                }
-                mt = fmaxf(pmj[0 * 128 + row], pmj[1 * 128 + row]) * sl2;
-                mn = fmaxf(m_run, mt);
-                need = mn > m_run + RESCALE_LOG2;
-                if (__any_sync(0xffffffffu, need)) {
-                    // the other half raised the max (rare): rescale this tile's P and sum
-                    f = need ? ex2(m_run - mn) : 1.f;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        pk0[e] = pack_bf16(__uint_as_float(pk0[e] << 16) * f, __uint_as_float(pk0[e] & 0xffff0000u) * f);
-                        pk1[e] = pack_bf16(__uint_as_float(pk1[e] << 16) * f, __uint_as_float(pk1[e] & 0xffff0000u) * f);
-                    }
-                    l0 *= f;
-                    l1 *= f;
-                    if (need) m_run = mn;
-                }
-            }
-            // P(j) may be written, and O rescaled, once PV(j-1) has completed
-            if (j > 0 && !waitw(BAR(B_PFREE), (j - 1) & 1, wc)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tO + 32u * c, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_st_x32(tO + 32u * c, o);
-                }
-            }
-            l_run = l_run * f + (l0 + l1);
-            tmem_st_x32(tP, pk0);
-            tmem_st_x32(tP + 32u, pk1);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PFULL));
-        }
-        if (ok && waitw(BAR(B_OFIN), 0, wc)) {
-            tc_fence_after();
+        for (int it = 0; ok; ++it) {
+            const int item = item_of(it);
+            if (item >= n_items) break;
+            const Item x = decode(item);
+            const Unit &w = x.w;
+            const int n = x.n;
+            const int qpos = w.q0 + row;
             const bool valid = qpos < w.cend;
+            if (n == 0) {
+                // A split or step with no key for the unit: this thread writes its
+                // row's half.  Split: the merge identity (out 0, lse -inf).  Step:
+                // merging changes nothing (out_final, if asked for, is the state
+                // rounded); a first step writes the empty state (out 0, lse -inf).
+                if constexpr (SPLIT) {
+                    if (valid) {
+                        const int64_t prow = (((int64_t)x.sp * a.B + w.b) * a.S + slot_pos(g, qpos)) * a.Hq + w.h;
+                        float4 *dst = reinterpret_cast<float4 *>(so.out + prow * D + (D / 2) * half);
+#pragma unroll
+                        for (int c4 = 0; c4 < D / 8; ++c4) dst[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (half == 0) so.lse[prow] = NEG_INF;
+                    }
+                } else if constexpr (STEP) {
+                    if (valid) {
+                        const int lr = dbg_coord(a.err, slot_lrow(g, w.r, qpos), C_loc);
+                        const int64_t srow = ((int64_t)w.b * C_loc + lr) * a.Hq + w.h;
+                        float4 *acc = reinterpret_cast<float4 *>(stp.out_acc + srow * D + (D / 2) * half);
+                        uint4 *fin = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(stp.out_final) +
+                                                               srow * D + (D / 2) * half);
+#pragma unroll
+                        for (int c8 = 0; c8 < D / 16; ++c8) {
+                            float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+                            if (stp.accumulate) {
+                                x0 = acc[2 * c8];
+                                x1 = acc[2 * c8 + 1];
+                            } else {
+                                acc[2 * c8] = x0;
+                                acc[2 * c8 + 1] = x1;
+                            }
+                            if (stp.out_final)
+                                fin[c8] = make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w),
+                                                     pack_bf16(x1.x, x1.y), pack_bf16(x1.z, x1.w));
+                        }
+                        if (!stp.accumulate && half == 0)
+                            stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + lr] = NEG_INF;
+                    }
+                }
+                continue;
+            }
+            float m_run = NEG_INF, l_run = 0.f;      // l_run: this half's share of the row sum
+
+            KvIter<KT> kit;
+            if (STEP)
+                kit.begin_steps(g, w.r, w.qmax, stp.step_k, stp.step_k + 1);
+            else
+                kit.begin(g, w.r, w.qmax);
+            if (SPLIT) kit.skip(x.j0);
+            for (int j = 0; j < n; ++j, ++nt, ++nx, kit.next()) {
+                if (!waitw(BAR(B_SFULL), nt & 1, wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sr[128];
+                tmem_ld_x128(tS, sr);
+                // S may now be overwritten: one arrival per warp (per-thread
+                // arrivals would serialise 256 atomics on one shared-memory word)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_SFREE));
+                float *s = reinterpret_cast<float *>(sr);
+                const int ks = kit.start();
+                const int kl = kit.len();
+                if (kl < KT || (a.causal && ks + kl - 1 > w.q0 + kit.shift)) {
+                    // partial tile: key columns [0, lim) of the 256 are visible to this row
+                    int lim = kl;
+                    if (a.causal) {
+                        const int c = qpos - ks + 1 + kit.shift;
+                        lim = c < lim ? c : lim;
+                    }
+                    lim -= 128 * half;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= lim) s[c] = NEG_INF;
+                }
+                // row max over this half: four independent 3-input max chains
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < 124; c += 8) {
+                    mx0 = fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+                }
+                mx0 = fmax3(mx0, s[124], s[125]);
+                mx1 = fmax3(mx1, s[126], s[127]);
+                mx0 = fmax3(mx0, mx2, mx3);
+                // Publish this half's row maximum (double-buffered by exchange
+                // parity; the barrier's phase completes once all 256 threads
+                // published theirs).
+                float *pmj = pm + (nx & 1) * 256;
+                const float mloc = fmaxf(mx0, mx1) * sl2;
+                pmj[half * 128 + row] = fmaxf(mx0, mx1);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_MX));
+                // The exponentials use the running max m_run as long as this half's own
+                // maximum stays within 2^8 of it (P <= 2^8, no overflow), so the exchange
+                // is off the critical path; the combined max is checked afterwards and,
+                // in the rare case it grew by more than 2^8, P is scaled down to the new
+                // max.  The first visible tile (m_run = -inf) and a half whose own max
+                // jumped take the exchanged max first.
+                const bool early = __any_sync(0xffffffffu, mloc > m_run + RESCALE_LOG2);
+                float mt = NEG_INF;
+                if (early) {
+                    if (!waitw(BAR(B_MX), nx & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    mt = fmaxf(pmj[0 * 128 + row], pmj[1 * 128 + row]) * sl2;
+                }
+                float mn = fmaxf(m_run, mt);
+                bool need = mn > m_run + RESCALE_LOG2;
+                float f = need ? ex2(m_run - mn) : 1.f;    // ex2(-inf) = 0 on the first tile
+                if (need) m_run = mn;
+                const float mu = (m_run == NEG_INF) ? 0.f : m_run;
+                // P = exp2(s*sl2 - mu), packed to bf16 as it is produced
+                float l0 = 0.f, l1 = 0.f;
+                uint32_t pk0[32], pk1[32];
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    float x0, x1;
+                    ffma2(x0, x1, s[c], s[c + 1], sl2, -mu);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    const uint32_t pk = pack_bf16(p0, p1);
+                    fadd2(l0, l1, p0, p1);
+                    if (c < 64) pk0[c / 2] = pk;
+                    else pk1[(c - 64) / 2] = pk;
+                }
+                if (!early) {
+                    if (!waitw(BAR(B_MX), nx & 1, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    mt = fmaxf(pmj[0 * 128 + row], pmj[1 * 128 + row]) * sl2;
+                    mn = fmaxf(m_run, mt);
+                    need = mn > m_run + RESCALE_LOG2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // the other half raised the max (rare): rescale this tile's P and sum
+                        f = need ? ex2(m_run - mn) : 1.f;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            pk0[e] = pack_bf16(__uint_as_float(pk0[e] << 16) * f, __uint_as_float(pk0[e] & 0xffff0000u) * f);
+                            pk1[e] = pack_bf16(__uint_as_float(pk1[e] << 16) * f, __uint_as_float(pk1[e] & 0xffff0000u) * f);
+                        }
+                        l0 *= f;
+                        l1 *= f;
+                        if (need) m_run = mn;
+                    }
+                }
+                // P may be written, and O rescaled, once the previous PV has
+                // completed (the previous unit's last one for j = 0)
+                if (nt > 0 && !waitw(BAR(B_PFREE), (nt - 1) & 1, wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_x32(tO + 32u * c, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_st_x32(tO + 32u * c, o);
+                    }
+                }
+                l_run = l_run * f + (l0 + l1);
+                tmem_st_x32(tP, pk0);
+                tmem_st_x32(tP + 32u, pk1);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_PFULL));
+            }
+            if (!ok || !waitw(BAR(B_OFIN), nu & 1, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
             // MODE_STEP: the running lse of the row, read by both halves before
             // the exchange below (half 0 overwrites it only after the exchange)
             float prev2 = NEG_INF;
@@ -549,13 +620,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     prev2 = stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, qpos)] *
                             1.4426950408889634f;
             }
-            // total row sum: this half's share plus the other's (exchange phase n;
-            // buffer n&1 was last read before the phase n-1 arrivals)
-            float *pmn = pm + (n & 1) * 256;
+            // total row sum: this half's share plus the other's (exchange nx;
+            // buffer nx&1 was last read before the arrivals of exchange nx-1)
+            float *pmn = pm + (nx & 1) * 256;
             pmn[half * 128 + row] = l_run;
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_MX));
-            ok = waitw(BAR(B_MX), n & 1, wc);
+            if (!waitw(BAR(B_MX), nx & 1, wc)) {
+                ok = false;
+                break;
+            }
+            ++nx;
             const float l_tot = pmn[row] + pmn[128 + row];
             const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const int qp = slot_pos(g, qpos);   // global position of the row
@@ -581,14 +656,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     wa = 1.f;
                     wb = 0.f;
                 }
-                const bool write = valid;
                 float *orow = stp.out_acc + srow * D + (D / 2) * half;
                 __nv_bfloat16 *frow = static_cast<__nv_bfloat16 *>(stp.out_final) + srow * D + (D / 2) * half;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     uint32_t o[32];
                     tmem_ld_x32(tO + 32u * c, o);
-                    if (write) {
+                    if (valid) {
                         float4 *dst = reinterpret_cast<float4 *>(orow + 32 * c);
                         uint4 *fdst = reinterpret_cast<uint4 *>(frow + 32 * c);
                         // 8 columns at a time: two float4 of state, one uint4 of bf16
@@ -616,12 +690,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                     }
                 }
-                if (ok && valid && !keep && half == 0)
+                if (valid && !keep && half == 0)
                     stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + slot_lrow(g, w.r, qpos)] =
                         new2 == NEG_INF ? NEG_INF : new2 * 0.69314718055994531f;
             } else if constexpr (SPLIT) {
                 const int64_t prow =
-                    (((int64_t)sp * a.B + w.b) * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h;
+                    (((int64_t)x.sp * a.B + w.b) * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h;
                 float *orow = so.out + prow * D + (D / 2) * half;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
@@ -635,32 +709,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                                   __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
                     }
                 }
-                if (ok && valid && half == 0)
+                if (valid && half == 0)
                     so.lse[prow] = l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
             } else {
-            __nv_bfloat16 *orow =
-                out + (((int64_t)w.b * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h) * D + (D / 2) * half;
+                __nv_bfloat16 *orow =
+                    out + (((int64_t)w.b * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h) * D + (D / 2) * half;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t o[32];
-                tmem_ld_x32(tO + 32u * c, o);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + 32u * c, o);
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 pkt;
-                        pkt.x = pack_bf16(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-                        pkt.y = pack_bf16(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-                        pkt.z = pack_bf16(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-                        pkt.w = pack_bf16(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                        dst[v4] = pkt;
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 pkt;
+                            pkt.x = pack_bf16(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                            pkt.y = pack_bf16(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                            pkt.z = pack_bf16(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                            pkt.w = pack_bf16(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                            dst[v4] = pkt;
+                        }
                     }
                 }
+                if (valid && half == 0)
+                    lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] =
+                        l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
             }
-            if (ok && valid && half == 0)
-                lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] =
-                    l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;
-            }
+            ++nu;
         }
         __syncwarp();
         tc_fence_before();
@@ -713,8 +788,20 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
                       kv_bytes > 48ll * 1024 * 1024) ? 1 : 0;
     const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
     if (units == 0) return CP_OK;
-    const int64_t blocks = units * (MODE == MODE_SPLIT ? so.n : 1);
-    if (blocks > 0x7fffffffLL) return CP_EUNSUPPORTED;
+    const int64_t items = units * (MODE == MODE_SPLIT ? so.n : 1);
+    if (items > 0x7fffffffLL) return CP_EUNSUPPORTED;
+    a.n_units = (int)units;
+    // One block per item while there are many items per SM: the hardware then
+    // hands blocks out longest first as SMs free up.  With few items per SM the
+    // fixed cost of a block (barrier set-up, tensor-memory allocation, the Q load
+    // and the pipeline fill before the first PV, the epilogue) weighs, so one
+    // persistent block per SM runs several items, loading the next unit's Q
+    // while the previous one finishes.
+    int64_t blocks = items;
+    const int64_t sms = sm_count();
+    if (items <= 16 * sms && items > sms) blocks = sms;
+    const int cap = fwd_grid_limit();   // test hook: the grid, overriding the rule above
+    if (cap > 0) blocks = items < cap ? items : cap;
     const float sl2 = a.scale * 1.4426950408889634f;
     fwd_bf16_kernel<D, MODE><<<(unsigned)blocks, NTHREADS, Cfg<D>::SMEM, st>>>(
         mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse, so, stp);

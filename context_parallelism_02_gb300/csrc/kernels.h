@@ -15,6 +15,7 @@ struct FwdArgs {
     int rank_lo, rank_hi; // virtual ranks whose queries are computed
     int upc;              // query units per chunk (set by the launcher)
     int head_grouped;     // units numbered with each (batch, head) contiguous (set by the launcher)
+    int n_units;          // query units of the launch (set by the launcher)
     unsigned *err;        // device error word
     uint64_t limit_ns;    // bound of every pipeline wait
     uint64_t drain_ns;    // bound of the waits that drain copies and MMAs before exit
@@ -88,5 +89,9 @@ int sm_count();
 unsigned *device_error_word();
 uint64_t device_wait_limit_ns();
 uint64_t device_drain_limit_ns();
+
+// Test hook: largest grid of the forward kernel (0: no limit), so that tests
+// can make every block run many work items.
+int fwd_grid_limit();
 
 }  // namespace cp

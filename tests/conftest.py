@@ -44,8 +44,23 @@ def bf16_bound(ref):
     return BF16_MAX + bf16_half_ulp(ref)
 
 
-# Absolute errors of every bf16 output check, reported at the end of the run.
+# Absolute errors of every bf16 output check, reported at the end of the run;
+# the same for gradients (with the largest reference entry) and fp32 outputs.
 ERRORS = []
+GRAD_ERRORS = []
+F32_ERRORS = []
+
+
+def record_grad(what, got, ref):
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    GRAD_ERRORS.append((str(what), float(err.max(initial=0)), float(err.mean()) if err.size else 0.0,
+                        float(np.abs(ref).max(initial=0))))
+
+
+def record_f32(what, out, ref, lse=None, lref=None):
+    err = np.abs(np.asarray(out, dtype=np.float64) - ref)
+    lerr = _lse_err(lse, lref).max(initial=0) if lse is not None else 0.0
+    F32_ERRORS.append((str(what), float(err.max(initial=0)), float(lerr)))
 
 
 def _lse_err(lse, lref):
@@ -86,7 +101,7 @@ def check_bf16_pair(a, b, what=""):
 
 
 def pytest_terminal_summary(terminalreporter):
-    if not ERRORS:
+    if not (ERRORS or GRAD_ERRORS or F32_ERRORS):
         return
     tr = terminalreporter
     tr.write_sep("-", "bf16 output errors against the fp64 oracle (absolute)")
@@ -94,6 +109,15 @@ def pytest_terminal_summary(terminalreporter):
                   f"{'max err/bound':>13s}")
     for what, mx, mean, lmx, ratio in ERRORS:
         tr.write_line(f"{what[:60]:60s} {mx:10.3e} {mean:10.3e} {lmx:12.3e} {ratio:13.3f}")
+    if GRAD_ERRORS:
+        tr.write_sep("-", "gradient errors against the fp64 oracle (absolute; bound 1e-2 / 1e-3 of max|ref|)")
+        tr.write_line(f"{'check':60s} {'max|err|':>10s} {'mean|err|':>10s} {'max|ref|':>10s}")
+        for what, mx, mean, ref in GRAD_ERRORS:
+            tr.write_line(f"{what[:60]:60s} {mx:10.3e} {mean:10.3e} {ref:10.3e}")
+    if F32_ERRORS:
+        tr.write_sep("-", "fp32 output errors against the fp64 oracle (absolute; bound 1e-5)")
+        for what, mx, lmx in F32_ERRORS:
+            tr.write_line(f"{what[:60]:60s} {mx:10.3e} {lmx:12.3e}")
 
 
 @pytest.fixture(scope="session")

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+from conftest import record_grad
 from context_parallelism_02_gb300 import api, inputs
 from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, STRIPED as STR, ZIGZAG as ZIG, Workload
 
@@ -33,6 +34,7 @@ def _grads(w, dev):
 
 
 def _check(name, got, ref):
+    record_grad(name, got, ref)
     err = np.abs(got - ref)
     scale = np.abs(ref).max()
     assert np.isfinite(got).all(), name

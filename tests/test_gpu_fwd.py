@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import F32_TOL, check_bf16, check_bf16_pair
+from conftest import F32_TOL, check_bf16, check_bf16_pair, record_f32
 from context_parallelism_02_gb300 import api, inputs
 from context_parallelism_02_gb300.inputs import CONTIGUOUS as CONT, STRIPED as STR, ZIGZAG as ZIG, Workload
 
@@ -38,6 +38,7 @@ def test_tiny_fp32(cuda_dev, oracle, layout, causal, qscale):
     w = inputs.TINY.with_(layout=layout, causal=causal, q_scale=qscale)
     q, k, v, out, lse = _run(w, cuda_dev)
     ref, lref = oracle.attn_fwd(q, k, v, causal)
+    record_f32(f"tiny fp32 layout {layout} causal {causal} q x {qscale}", out, ref, lse, lref)
     assert np.abs(out - ref).max() <= F32_TOL
     assert np.abs(lse - lref).max() <= F32_TOL
 
