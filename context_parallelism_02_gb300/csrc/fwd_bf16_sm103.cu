@@ -143,7 +143,10 @@ __device__ __forceinline__ void issue_pv_seq(uint32_t tO, uint32_t tP, uint64_t 
 //               rescaling, and optionally written rounded to bf16.
 enum { MODE_RING = 0, MODE_SPLIT = 1, MODE_STEP = 2 };
 
-template <int D, int MODE>
+// PERSIST: the block runs several work items in turn (fewer blocks than
+// items); otherwise it runs item blockIdx.x alone and its item loops run once,
+// so every running count below folds to the per-unit index.
+template <int D, int MODE, bool PERSIST>
 __global__ void __launch_bounds__(NTHREADS, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs a, const float sl2,
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // numbering, so the blocks' totals stay close.  With one block per item
     // (gridDim.x == n_items) the block runs item blockIdx.x alone.
     auto item_of = [&](int it) -> int {
+        if (!PERSIST) return it == 0 ? (int)blockIdx.x : n_items;
         const int64_t G = gridDim.x, c = blockIdx.x;
         const int64_t item = it * G + ((it & 1) ? G - 1 - c : c);
         return item < n_items ? (int)item : n_items;
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
             int nq = 0, nk = 0, nv = 0;   // Q loads, K tiles, V halves issued so far
             bool ok = true;
-            for (int it = 0; ok; ++it) {
+            for (int it = 0; ok && (PERSIST || it == 0); ++it) {
                 const int item = item_of(it);
                 if (item >= n_items) break;
                 const Item x = decode(item);
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (warp == 1) {
                 const uint64_t dQ = sdesc(sQ, 16, 1024);
                 const uint64_t dK0 = sdesc(sK, 16, 1024);
-                for (int it = 0; ok; ++it) {
+                for (int it = 0; ok && (PERSIST || it == 0); ++it) {
                     const int item = item_of(it);
                     if (item >= n_items) break;
                     const int n = decode(item).n;
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             } else {
                 const uint64_t dV0 = sdesc(sV, 16384, 1024);
-                for (int it = 0; ok; ++it) {
+                for (int it = 0; ok && (PERSIST || it == 0); ++it) {
                     const int item = item_of(it);
                     if (item >= n_items) break;
                     const int n = decode(item).n;
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool ok = true;
         int nu = 0, nt = 0, nx = 0;   // units finished, tiles done, row-max exchanges so far
 
-        for (int it = 0; ok; ++it) {
+        for (int it = 0; ok && (PERSIST || it == 0); ++it) {
             const int item = item_of(it);
             if (item >= n_items) break;
             const Item x = decode(item);
@@ -769,7 +773,9 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CP_ECUDA;
     if (dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(fwd_bf16_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(fwd_bf16_kernel<D, MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg<D>::SMEM) != cudaSuccess ||
+            cudaFuncSetAttribute(fwd_bf16_kernel<D, MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<D>::SMEM) != cudaSuccess)
             return CP_ECUDA;
         attr_done[dev] = true;
@@ -797,14 +803,20 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
     // and the pipeline fill before the first PV, the epilogue) weighs, so one
     // persistent block per SM runs several items, loading the next unit's Q
     // while the previous one finishes.
+    // (A split launch already spreads long rows over blocks; it keeps one
+    // block per item.)
     int64_t blocks = items;
     const int64_t sms = sm_count();
-    if (items <= 16 * sms && items > sms) blocks = sms;
+    if (MODE != MODE_SPLIT && items <= 16 * sms && items > sms) blocks = sms;
     const int cap = fwd_grid_limit();   // test hook: the grid, overriding the rule above
     if (cap > 0) blocks = items < cap ? items : cap;
     const float sl2 = a.scale * 1.4426950408889634f;
-    fwd_bf16_kernel<D, MODE><<<(unsigned)blocks, NTHREADS, Cfg<D>::SMEM, st>>>(
-        mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse, so, stp);
+    if (blocks < items)
+        fwd_bf16_kernel<D, MODE, true><<<(unsigned)blocks, NTHREADS, Cfg<D>::SMEM, st>>>(
+            mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse, so, stp);
+    else
+        fwd_bf16_kernel<D, MODE, false><<<(unsigned)blocks, NTHREADS, Cfg<D>::SMEM, st>>>(
+            mq, mk, mv, a, sl2, reinterpret_cast<__nv_bfloat16 *>(out), lse, so, stp);
     return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ECUDA;
 }
 

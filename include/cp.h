@@ -385,8 +385,8 @@ int cp_debug_set_wait_limit(uint64_t limit_ns);
  * cp_debug_set_grid_limit -- test hook: the tensor-core forward (ring, split
  * and step modes) launches min(work items, max_blocks) thread blocks from now
  * on in this process, each running its share of the items in turn (0 restores
- * the default grid: one block per item, or one per SM when there are at most
- * 16 items per SM).  Results do not depend on the grid: every item is
+ * the default grid: one block per item, or, for ring and step launches with
+ * at most 16 items per SM, one block per SM).  Results do not depend on the grid: every item is
  * computed the same way whichever block runs it.  Process-wide; not for use
  * while other threads launch work.  Errors: CP_EINVAL for max_blocks < 0.
  * Host only.
