@@ -783,7 +783,10 @@ def main():
     # another (the host link is full duplex), ordered by events, so that the
     # copies of step i+1 and i-1 overlap the forward of step i.  All copies of
     # the timed steps lie inside the timed region.
-    e2e_steps = max(3, min(args.steps, 10))
+    # as many pipelined steps as the timed region (at least 3): the first
+    # upload and the last read-back of a repetition cannot overlap a forward,
+    # and more steps spread them thinner
+    e2e_steps = max(3, min(args.steps, 50))
     ins = [(q, k, v), tuple(torch.empty_like(t) for t in (q, k, v))]
     outs = [(out, lse), (torch.empty_like(out), torch.empty_like(lse))]
     outs_h = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in o) for o in outs]
@@ -831,12 +834,12 @@ def main():
     e2e_sampler = ClockSampler(local, getattr(torch.cuda.get_device_properties(dev), "uuid", None)
                                and "GPU-" + str(torch.cuda.get_device_properties(dev).uuid), 50)
     e2e_sampler.start()
-    # five repetitions of the pipelined steps, each with all its copies inside
+    # three repetitions of the pipelined steps, each with all its copies inside
     # its own timed region; the median is reported (the host link of these
     # boxes drops for a while now and then from ~208 GB/s to ~15 GB/s, and a
     # repetition that catches such a drop is copy-bound)
     e2e_all, fwd_only_all = [], []
-    for _ in range(5):
+    for _ in range(3):
         # the same forward with inputs already in HBM, timed right before the
         # end-to-end steps, so both see the same clocks and power state
         t0.record(stream)
