@@ -855,6 +855,26 @@ def main():
         torch.cuda.synchronize()
         e2e_all.append(t0.elapsed_time(t1) / e2e_steps)
     e2e_clocks = e2e_sampler.stop()
+    # what the copies do to the forward: one forward with the next step's whole
+    # upload running beside it on the copy stream, against the same forward
+    # and the upload alone (CUDA events; medians of three)
+    conc = {"fwd_alone": [], "fwd_with_upload": [], "upload_alone": []}
+    for _ in range(3):
+        for key in conc:
+            torch.cuda.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            up.wait_event(a0)
+            if key != "upload_alone":
+                step()
+            if key != "fwd_alone":
+                with torch.cuda.stream(up):
+                    upload(1)
+            stream.wait_stream(up)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            conc[key].append(a0.elapsed_time(a1))
     assert api.cp_get_error() == 0
     e2e_ms = max_over_ranks(statistics.median(e2e_all), world, dev)
     fwd_only_ms = max_over_ranks(statistics.median(fwd_only_all), world, dev)
@@ -905,6 +925,9 @@ def main():
                 "link_h2d_gbs": link["h2d"], "link_d2h_gbs": link["d2h"],
                 "link_h2d_gbs_min": link["h2d_min"], "link_d2h_gbs_min": link["d2h_min"],
                 "copy_ms_per_step": h2d / link["h2d"] / 1e6 + d2h / link["d2h"] / 1e6,
+                "fwd_alone_ms": statistics.median(conc["fwd_alone"]),
+                "fwd_with_concurrent_upload_ms": statistics.median(conc["fwd_with_upload"]),
+                "upload_alone_ms": statistics.median(conc["upload_alone"]),
                 "sm_mhz": e2e_clocks.get("sm_mhz"),
                 "power_w_max": e2e_clocks.get("power_w_max"),
                 "reasons": ",".join(e2e_clocks.get("reasons", [])),
