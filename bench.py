@@ -200,7 +200,7 @@ def run_reference(args, w, rank):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(w, args.workload),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample_desc},
@@ -606,6 +606,7 @@ def ring_measure(q, k, v, *, rank, world, S, layout, causal, steps, warmup, tran
 def main_ring(args, w, world, rank, local, dev, stream, peaks):
     """N > 1: the GPUs of the job form one ring over the workload's sequence."""
     import torch
+    import torch.distributed as dist
     from context_parallelism_02_gb300 import api, inputs, ring
     wl = w.with_(N=world)
     q, k, v = inputs.make_qkv(wl)
@@ -613,8 +614,12 @@ def main_ring(args, w, world, rank, local, dev, stream, peaks):
     qs, ks, vs = (ring.shard(x, rank, world, pos_layout).to(dev) for x in (q, k, v))
     blocks = [tuple(ring.shard(x, r, world, pos_layout).to(dev) for x in (k, v)) for r in range(world)]
     del q, k, v
-    transport = ring.P2PTransport()
-    sampler = ClockSampler(local)
+    # NCCL moves the blocks GPU to GPU; over a gloo group (CP_BENCH_BACKEND=gloo,
+    # e.g. several ranks sharing one GPU in a test) they go through pinned host
+    # memory
+    transport = (ring.P2PTransport() if dist.get_backend() == "nccl"
+                 else ring.HostStagedTransport())
+    sampler = ClockSampler(dev.index)
     sampler.start()
     m = ring_measure(qs, ks, vs, rank=rank, world=world, S=wl.S, layout=wl.layout,
                      causal=wl.causal, steps=args.steps, warmup=args.warmup,
@@ -673,6 +678,8 @@ def max_over_ranks(x, world, device):
     """Max of a per-rank float over all ranks (identity with one rank)."""
     import torch
     import torch.distributed as dist
+    if world > 1 and dist.get_backend() == "gloo":
+        device = "cpu"   # gloo reduces host tensors
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -716,10 +723,15 @@ def main():
     from context_parallelism_02_gb300 import api, build, inputs
 
     build.build()
-    dev = torch.device("cuda", local)
+    # one GPU per rank; ranks beyond the visible GPUs share them (tests only)
+    dev = torch.device("cuda", local % max(1, torch.cuda.device_count()))
     torch.cuda.set_device(dev)
     if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
+        backend = os.environ.get("CP_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=dev)
+        else:
+            dist.init_process_group(backend)
     peaks, peak_src = load_peaks()
     # one ordinary stream for all work of this process (the legacy default
     # stream would order itself against the end-to-end copy streams)
@@ -904,7 +916,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q, k, v drawn on the host)",
         "config": config_of(w, args.workload),
         "pct_of_bf16_peak": 100.0 * achieved / peak,
