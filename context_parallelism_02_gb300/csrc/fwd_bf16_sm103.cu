@@ -14,8 +14,15 @@
 // Work unit: one 128-row query tile of one chunk and one (batch, query head),
 // walking 256-key tiles.  S = Q K^T is issued as M=128, N=256 MMAs: on this
 // part an N=128 MMA pays a fixed overhead (about 90 cycles for 64 cycles of
-// work) that an N=256 one hides.  Units are launched in descending query
+// work) that an N=256 one hides.  Units are numbered in descending query
 // position, which under a causal mask is descending work.
+//
+// Modes (template parameter): the ring over global-order tensors; split-KV
+// partials (a unit's walk cut into pieces, each written in fp32 for a merge
+// kernel); and one ring step on shard-local buffers (flash_block_step),
+// merged into a running (out, lse) state.  A launch either runs one block
+// per work item, or (PERSIST, few items per SM) one block per SM taking its
+// items in turn, with every barrier phase a running count across items.
 //
 // Roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q once; K tiles (256 rows) into a 2-deep ring

@@ -32,9 +32,12 @@
  *     reference after the call returns).  They must be 16-byte aligned.
  *   - stream is a cudaStream_t (NULL = legacy default stream).  Compute calls
  *     are asynchronous on it and return after the launch.
- *   - The library allocates no device memory.  It reports device-side
- *     failures (a bounded wait that timed out) through a per-device error word
- *     read by cp_get_error().
+ *   - The library allocates no device memory (its only device state is a
+ *     per-device error word and the fixed scratch of ring_attn_bwd_noalloc,
+ *     both compiled in).  It reports device-side failures (a bounded wait that
+ *     timed out, a misaligned shared-memory base, and in the debug-bounds
+ *     build an out-of-range tile coordinate) through the error word, read by
+ *     cp_get_error().
  *   - Return value: CP_OK or a negative CP_E* code; never an exception.
  */
 #ifndef CP_H_
