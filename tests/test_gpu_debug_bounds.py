@@ -48,8 +48,18 @@ def test_forward_backward_in_bounds(debug_bounds, oracle, cuda_dev, case):
     osp, lsp = api.ring_attn_fwd_split(gq, gk, gv, N, layout, causal, n_split=3)
     ost, lst = ring.ring_attention_emulated(gq, gk, gv, N, layout, causal)
     dq, dk, dv = api.ring_attn_bwd(gq, gk, gv, out, lse, gdo, N, layout, causal)
-    torch.cuda.synchronize()
+    # the persistent instantiations too: 3 blocks take every item in turn
+    api.cp_debug_set_grid_limit(3)
+    try:
+        outp, lsep = api.ring_attn_fwd(gq, gk, gv, N, layout, causal)
+        ospp, _ = api.ring_attn_fwd_split(gq, gk, gv, N, layout, causal, n_split=3)
+        ostp, _ = ring.ring_attention_emulated(gq, gk, gv, N, layout, causal)
+        torch.cuda.synchronize()
+    finally:
+        api.cp_debug_set_grid_limit(0)
     assert api.cp_get_error() == 0          # in particular no CP_EBOUNDS
+    assert torch.equal(outp, out) and torch.equal(lsep, lse)
+    assert torch.equal(ospp, osp) and torch.equal(ostp, ost)
     ref, lref = oracle.attn_fwd(q, k, v, causal)
     for tag, o, l_ in (("ring", out, lse), ("split", osp, lsp), ("step", ost, lst)):
         check_bf16(o.float().cpu().numpy(), l_.cpu().numpy(), ref, lref, f"debug-bounds {name} {tag}")
