@@ -226,10 +226,12 @@ struct KvIter {
             if (t >= nt) advance_chunk();
         }
     }
-    // Total tiles of the walk over ring steps [k0, k1) (closed form per chunk).
+    // Total tiles of the walk over ring steps [k0, k1) (closed form per chunk;
+    // the whole ring in closed form, see ring_count).
     CP_HD static int count(const Geom &g, int r, int qmax, int k0 = 0, int k1 = -1)
     {
         if (k1 < 0) k1 = g.N;
+        if (k0 == 0 && k1 == g.N) return ring_count(g, r, qmax);
         int n = 0;
         for (int k = k0; k < k1; ++k) {
             int src = ring_source(g.N, r, k);
@@ -238,6 +240,27 @@ struct KvIter {
                                         qmax + diag_shift(g, r, src));
         }
         return n;
+    }
+    // The whole ring (steps 0..N-1) holds every chunk of the sequence exactly
+    // once, so the per-step sum collapses.  Contiguous and zigzag (no diagonal
+    // shift): the chunks below the one holding qmax are visible in full, that
+    // chunk up to qmax, the chunks above it not at all.  Striped: the chunk of
+    // source src shows its local rows up to t - [src > r], t the local row of
+    // qmax, for the r + 1 sources src <= r and the N - 1 - r sources above.
+    CP_HD static int ring_count(const Geom &g, int r, int qmax)
+    {
+        const int ntiles = (g.clen + TILE - 1) / TILE;
+        if (!g.causal) return g.N * g.cpr * ntiles;
+        if (!striped(g)) {
+            const int cq = qmax / g.clen;
+            const int part = (qmax - cq * g.clen) / TILE + 1;
+            return cq * ntiles + (part < ntiles ? part : ntiles);
+        }
+        const int t = qmax - r * g.clen;
+        int lo = t / TILE + 1, hi = t >= 1 ? (t - 1) / TILE + 1 : 0;
+        lo = lo < ntiles ? lo : ntiles;
+        hi = hi < ntiles ? hi : ntiles;
+        return (r + 1) * lo + (g.N - 1 - r) * hi;
     }
 };
 

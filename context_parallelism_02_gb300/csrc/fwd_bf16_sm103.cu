@@ -330,17 +330,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(B_KFULL + (j & 1)), (j >> 1) & 1, dc);
                 for (int x = nv > 2 ? nv - 2 : 0; x < nv; ++x) wait1(BAR(B_VFULL + (x & 1)), (x >> 1) & 1, dc);
             }
-        } else if ((warp == 1 || warp == 2) && lane == 0) {
+        } else if (warp == 1 || warp == 2) {
             // ------------------------------------------------------------ MMA issuers
-            // Two issuing threads on different SM sub-partitions: warp 1 issues
+            // Two issuing warps on different SM sub-partitions: warp 1 issues
             // S = Q K^T, warp 2 issues O += P V.  They touch disjoint tensor-memory
             // columns (S vs P and O); every dependency between them goes through
             // the softmax barriers (S_FREE, P_FULL, P_FREE).  Splitting halves the
             // issue work each one competes for against two busy softmax warps, and
-            // a wait of one issuer never holds back the other.
+            // a wait of one issuer never holds back the other.  Each warp runs
+            // converged (warp-collective waits), so its operands stay warp-uniform,
+            // and one elected lane issues the MMAs and their commits.
             constexpr uint32_t idS = idesc_bf16(128, KT, false);
             constexpr uint32_t idO = idesc_bf16(128, D, true);
             const uint32_t tS = tmem, tP = tmem + 256u, tO = tmem + 384u;
+            const bool leader = elect_one();
             bool ok = true;
             int nq = 0, nt = 0;   // units started, tiles issued so far
             if (warp == 1) {
@@ -351,26 +354,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (item >= n_items) break;
                     const int n = decode(item).n;
                     if (n == 0) continue;
-                    if (!wait1(BAR(B_Q), nq & 1, wc)) break;
+                    if (!waitw(BAR(B_Q), nq & 1, wc)) break;
                     for (int j = 0; j < n; ++j, ++nt) {
                         const int st = nt & 1;
-                        if ((nt > 0 && !wait1(BAR(B_SFREE), (nt - 1) & 1, wc)) ||
-                            !wait1(BAR(B_KFULL + st), (nt >> 1) & 1, wc)) {
+                        if ((nt > 0 && !waitw(BAR(B_SFREE), (nt - 1) & 1, wc)) ||
+                            !waitw(BAR(B_KFULL + st), (nt >> 1) & 1, wc)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        issue_s_seq<0, D>(tS, dQ, dK0 + (uint64_t)(st * (C::KBYTES >> 4)), idS);
-                        mma_commit(BAR(B_SFULL));
-                        mma_commit(BAR(B_KEMPTY + st));
+                        const uint64_t dK = dK0 + (uint64_t)(st * (C::KBYTES >> 4));
+                        if (leader) {
+                            tc_fence_after();
+                            issue_s_seq<0, D>(tS, dQ, dK, idS);
+                            mma_commit(BAR(B_SFULL));
+                            mma_commit(BAR(B_KEMPTY + st));
+                        }
+                        __syncwarp();
                     }
                     if (!ok) break;
                     // Q may be reloaded once the unit's S MMAs have completed
-                    mma_commit(BAR(B_QEMPTY));
+                    if (leader) mma_commit(BAR(B_QEMPTY));
+                    __syncwarp();
                     ++nq;
                 }
             } else {
                 const uint64_t dV0 = sdesc(sV, 16384, 1024);
+                const uint64_t dV1 = dV0 + (uint64_t)(C::VBYTES >> 4);
                 for (int it = 0; ok && (PERSIST || it == 0); ++it) {
                     const int item = item_of(it);
                     if (item >= n_items) break;
@@ -379,35 +388,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         // P(nt) written: every softmax warp has also finished reading
                         // the previous unit's O, which the first PV of this unit
                         // (accumulate 0) overwrites
-                        if (!wait1(BAR(B_PFULL), nt & 1, wc)) {
+                        if (!waitw(BAR(B_PFULL), nt & 1, wc) || !waitw(BAR(B_VFULL + 0), nt & 1, wc)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        for (int hh = 0; hh < 2; ++hh) {
-                            if (!wait1(BAR(B_VFULL + hh), nt & 1, wc)) {
-                                ok = false;
-                                break;
-                            }
+                        const uint32_t acc0 = j > 0 ? 1u : 0u;
+                        if (leader) {
                             tc_fence_after();
-                            if (hh == 0)
-                                issue_pv_seq<0, 0>(tO, tP, dV0, idO, j > 0 ? 1u : 0u);
-                            else
-                                issue_pv_seq<0, 1>(tO, tP, dV0 + (uint64_t)(C::VBYTES >> 4), idO, 1u);
-                            mma_commit(BAR(B_VEMPTY + hh));
+                            issue_pv_seq<0, 0>(tO, tP, dV0, idO, acc0);
+                            mma_commit(BAR(B_VEMPTY + 0));
                         }
-                        if (!ok) break;
-                        mma_commit(BAR(B_PFREE));
-                        if (j + 1 == n) mma_commit(BAR(B_OFIN));
+                        __syncwarp();
+                        if (!waitw(BAR(B_VFULL + 1), nt & 1, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        if (leader) {
+                            tc_fence_after();
+                            issue_pv_seq<0, 1>(tO, tP, dV1, idO, 1u);
+                            mma_commit(BAR(B_VEMPTY + 1));
+                            mma_commit(BAR(B_PFREE));
+                            if (j + 1 == n) mma_commit(BAR(B_OFIN));
+                        }
+                        __syncwarp();
                     }
                 }
             }
-            // all MMAs of this thread are complete once the drain barrier (two
+            // all MMAs of this warp are complete once the drain barrier (two
             // arrivals: one commit per issuer) fires
-            mma_commit(BAR(B_DRAIN));
+            if (leader) mma_commit(BAR(B_DRAIN));
+            __syncwarp();
             volatile int no_abort = 0;
             WaitCtl dc{a.err, &no_abort, a.drain_ns};
-            wait1(BAR(B_DRAIN), 0, dc);
+            waitw(BAR(B_DRAIN), 0, dc);
         }
         // end of warpgroup 0: wait for every role, then warp 0 frees tensor memory
         __syncwarp();

@@ -88,6 +88,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
         : "memory");
 }
 
+// One lane of a converged warp (elect.sync: the lowest active lane).  A warp
+// that runs its control flow converged keeps its MMA operands (descriptors,
+// tensor-memory addresses, loop counters) warp-uniform, and only the elected
+// lane issues.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
