@@ -325,55 +325,71 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 wait1(BAR(Q_DOFULL), 0, dc);
                 for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) wait1(BAR(Q_VFULL + (j & 1)), (j >> 1) & 1, dc);
             }
-        } else if ((warp == 1 || warp == 2) && lane == 0) {
+        } else if (warp == 1 || warp == 2) {
             // ------------------------------------------------------------ MMA issuers
             // warp 1: S = Q K^T (A = Q from tensor memory) and dP = dO V^T;
-            // warp 2: dQ += dS K.
+            // warp 2: dQ += dS K.  Each warp runs converged (warp-collective
+            // waits), so its operands stay warp-uniform, and one elected lane
+            // issues the MMAs and their commits.
             constexpr uint32_t idSP = idesc_bf16(128, T, false);     // K-major A and B
             constexpr uint32_t idDQ = idesc_bf16(128, D, true);      // B = K MN-major
             const uint32_t tS = tmem + C::TM_S, tP = tmem + C::TM_P, tDQ = tmem + C::TM_DQ,
                            tDS = tmem + C::TM_DS;
+            const bool leader = elect_one();
             bool ok = true;
             if (warp == 1) {
                 const uint64_t dDOd = sdesc(sDO, 16, 1024), dQd = sdesc(sQ, 16, 1024);
                 const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, 16, 1024);
-                ok = wait1(BAR(Q_QTM), 0, wc) && wait1(BAR(Q_DOFULL), 0, wc);
+                ok = waitw(BAR(Q_QTM), 0, wc) && waitw(BAR(Q_DOFULL), 0, wc);
                 Ring<Q_KST> kr;
                 for (int j = 0; ok && j < n; ++j, kr.next()) {
                     const int sv = j & 1;
-                    if ((j > 0 && !wait1(BAR(Q_SFREE), (j - 1) & 1, wc)) ||
-                        !wait1(BAR(Q_KFULL + kr.st), kr.ph, wc))
+                    if ((j > 0 && !waitw(BAR(Q_SFREE), (j - 1) & 1, wc)) ||
+                        !waitw(BAR(Q_KFULL + kr.st), kr.ph, wc))
                         break;
-                    tc_fence_after();
-                    ss_seq<0, D, 16384>(tS, dQd, dK0 + (uint64_t)(kr.st * (TB >> 4)), idSP);
-                    mma_commit(BAR(Q_SDONE));
-                    mma_commit(BAR(Q_KEMPTY + kr.st));
-                    if ((j > 0 && !wait1(BAR(Q_PFREE), (j - 1) & 1, wc)) ||
-                        !wait1(BAR(Q_VFULL + sv), (j >> 1) & 1, wc))
+                    const uint64_t dK = dK0 + (uint64_t)(kr.st * (TB >> 4));
+                    if (leader) {
+                        tc_fence_after();
+                        ss_seq<0, D, 16384>(tS, dQd, dK, idSP);
+                        mma_commit(BAR(Q_SDONE));
+                        mma_commit(BAR(Q_KEMPTY + kr.st));
+                    }
+                    __syncwarp();
+                    if ((j > 0 && !waitw(BAR(Q_PFREE), (j - 1) & 1, wc)) ||
+                        !waitw(BAR(Q_VFULL + sv), (j >> 1) & 1, wc))
                         break;
-                    tc_fence_after();
-                    ss_seq<0, D, 16384>(tP, dDOd, dV0 + (uint64_t)(sv * (TB >> 4)), idSP);
-                    mma_commit(BAR(Q_PDONE));
-                    mma_commit(BAR(Q_VEMPTY + sv));
+                    const uint64_t dV = dV0 + (uint64_t)(sv * (TB >> 4));
+                    if (leader) {
+                        tc_fence_after();
+                        ss_seq<0, D, 16384>(tP, dDOd, dV, idSP);
+                        mma_commit(BAR(Q_PDONE));
+                        mma_commit(BAR(Q_VEMPTY + sv));
+                    }
+                    __syncwarp();
                 }
             } else {
                 const uint64_t dKmn0 = sdesc(sK, 16384, 1024);
                 Ring<Q_KST> kr;
                 for (int j = 0; ok && j < n; ++j, kr.next()) {
-                    if (!wait1(BAR(Q_DS), j & 1, wc) || !wait1(BAR(Q_KFULL + kr.st), kr.ph, wc))
+                    if (!waitw(BAR(Q_DS), j & 1, wc) || !waitw(BAR(Q_KFULL + kr.st), kr.ph, wc))
                         break;
-                    tc_fence_after();
-                    ts_mn_seq<0, T / 16, 0>(tDQ, tDS, dKmn0 + (uint64_t)(kr.st * (TB >> 4)), idDQ,
-                                            j > 0 ? 1u : 0u);
-                    mma_commit(BAR(Q_KEMPTY + kr.st));
-                    mma_commit(BAR(Q_DSFREE));
-                    if (j + 1 == n) mma_commit(BAR(Q_FIN));
+                    const uint64_t dK = dKmn0 + (uint64_t)(kr.st * (TB >> 4));
+                    const uint32_t acc0 = j > 0 ? 1u : 0u;
+                    if (leader) {
+                        tc_fence_after();
+                        ts_mn_seq<0, T / 16, 0>(tDQ, tDS, dK, idDQ, acc0);
+                        mma_commit(BAR(Q_KEMPTY + kr.st));
+                        mma_commit(BAR(Q_DSFREE));
+                        if (j + 1 == n) mma_commit(BAR(Q_FIN));
+                    }
+                    __syncwarp();
                 }
             }
-            mma_commit(BAR(Q_DRAIN));
+            if (leader) mma_commit(BAR(Q_DRAIN));
+            __syncwarp();
             volatile int no_abort = 0;
             WaitCtl dc{a.err, &no_abort, a.drain_ns};
-            wait1(BAR(Q_DRAIN), 0, dc);
+            waitw(BAR(Q_DRAIN), 0, dc);
         }
         __syncwarp();
         tc_fence_before();
@@ -673,29 +689,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int s = issued > K_QST ? issued - K_QST : 0; s < issued; ++s)
                     wait1(BAR(K_QFULL + s % K_QST), (s / K_QST) & 1, dc);
             }
-        } else if ((warp == 1 || warp == 2) && lane == 0) {
+        } else if (warp == 1 || warp == 2) {
             // ------------------------------------------------------------ MMA issuers
-            // tcgen05.mma issue returns only once the MMAs are nearly done, so a
-            // single issuing thread leaves the tensor pipe idle while it waits on
-            // a barrier.  Two threads: warp 2 issues S^T/dP^T(s) into buffer s%2
-            // once dV/dK(s-2) has finished reading it; warp 1 issues dV/dK(s) once
-            // the gradient warpgroup has written P^T(s) and dS^T(s).
-            bool ok = wait1(BAR(K_KVFULL), 0, wc);
+            // Two issuing warps, so that a wait of one never leaves the tensor
+            // pipe without work from the other: warp 2 issues S^T/dP^T(s) into
+            // buffer s%2 once dV/dK(s-2) has finished reading it; warp 1 issues
+            // dV/dK(s) once the gradient warpgroup has written P^T(s) and dS^T(s).
+            // Each warp runs converged (warp-collective waits), so its operands
+            // stay warp-uniform, and one elected lane issues the MMAs and commits.
+            const bool leader = elect_one();
+            bool ok = waitw(BAR(K_KVFULL), 0, wc);
             if (warp == 2) {
                 constexpr uint32_t idSP = idesc_bf16(128, 64, false);   // N = 64 queries
                 const uint64_t dKd = sdesc(sK, 16, 1024), dVd = sdesc(sV, 16, 1024);
                 const uint64_t dQ0 = sdesc(sQ, 16, 1024);               // Q_s K-major (64-row boxes)
                 Ring<K_QST> rs;
                 for (int s = 0; ok && s < ns; ++s, rs.next()) {
-                    if ((s >= 2 && !wait1(BAR(K_BUF + (s & 1)), ((s >> 1) - 1) & 1, wc)) ||
-                        !wait1(BAR(K_QFULL + rs.st), rs.ph, wc))
+                    if ((s >= 2 && !waitw(BAR(K_BUF + (s & 1)), ((s >> 1) - 1) & 1, wc)) ||
+                        !waitw(BAR(K_QFULL + rs.st), rs.ph, wc))
                         break;
-                    tc_fence_after();
                     const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
                     const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
-                    ss_seq<0, D, 8192>(tb, dKd, dQ0 + so, idSP);
-                    ss_seq<0, D, 8192>(tb + 64u, dVd, dQ0 + so + (uint64_t)(HB >> 4), idSP);
-                    mma_commit(BAR(K_SDP + (s & 1)));
+                    if (leader) {
+                        tc_fence_after();
+                        ss_seq<0, D, 8192>(tb, dKd, dQ0 + so, idSP);
+                        ss_seq<0, D, 8192>(tb + 64u, dVd, dQ0 + so + (uint64_t)(HB >> 4), idSP);
+                        mma_commit(BAR(K_SDP + (s & 1)));
+                    }
+                    __syncwarp();
                 }
             } else {
                 constexpr uint32_t idKV = idesc_bf16(128, D, true);     // dV, dK: B MN-major
@@ -703,27 +724,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t tDV = tmem + C::TM_DV, tDK = tmem + C::TM_DK;
                 Ring<K_QST> rs;
                 for (int s = 0; ok && s < ns; ++s, rs.next()) {
-                    if (!wait1(BAR(K_PW + (s & 1)), (s >> 1) & 1, wc)) break;
-                    tc_fence_after();
+                    if (!waitw(BAR(K_PW + (s & 1)), (s >> 1) & 1, wc)) break;
                     const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
                     const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
+                    const uint32_t acc0 = s > 0 ? 1u : 0u;
                     // dV += P^T dO_s as soon as P^T is written, while the gradient
                     // warps compute dS^T; then dK += dS^T Q_s (K = 64 queries: 4 MMAs each)
-                    ts_mn_seq<0, 4, 0>(tDV, tb, dQmn0 + so + (uint64_t)(HB >> 4), idKV, s > 0 ? 1u : 0u);
-                    if (!wait1(BAR(K_DSW + (s & 1)), (s >> 1) & 1, wc)) break;
-                    tc_fence_after();
-                    ts_mn_seq<0, 4, 0>(tDK, tb + 64u, dQmn0 + so, idKV, s > 0 ? 1u : 0u);
-                    // S^T/dP^T(s) completed before the gradient warps started, so the
-                    // stage is free once dV/dK(s) completes
-                    mma_commit(BAR(K_QEMPTY + rs.st));
-                    mma_commit(BAR(K_BUF + (s & 1)));
+                    if (leader) {
+                        tc_fence_after();
+                        ts_mn_seq<0, 4, 0>(tDV, tb, dQmn0 + so + (uint64_t)(HB >> 4), idKV, acc0);
+                    }
+                    __syncwarp();
+                    if (!waitw(BAR(K_DSW + (s & 1)), (s >> 1) & 1, wc)) break;
+                    if (leader) {
+                        tc_fence_after();
+                        ts_mn_seq<0, 4, 0>(tDK, tb + 64u, dQmn0 + so, idKV, acc0);
+                        // S^T/dP^T(s) completed before the gradient warps started, so the
+                        // stage is free once dV/dK(s) completes
+                        mma_commit(BAR(K_QEMPTY + rs.st));
+                        mma_commit(BAR(K_BUF + (s & 1)));
+                    }
+                    __syncwarp();
                 }
-                mma_commit(BAR(K_FIN));
+                if (leader) mma_commit(BAR(K_FIN));
+                __syncwarp();
             }
-            mma_commit(BAR(K_DRAIN));
+            if (leader) mma_commit(BAR(K_DRAIN));
+            __syncwarp();
             volatile int no_abort = 0;
             WaitCtl dc{a.err, &no_abort, a.drain_ns};
-            wait1(BAR(K_DRAIN), 0, dc);
+            waitw(BAR(K_DRAIN), 0, dc);
         }
         __syncwarp();
         tc_fence_before();

@@ -588,11 +588,20 @@ static __device__ __forceinline__ bool waitw_slow(uint32_t bar, uint32_t parity,
     }
 }
 
+// First probe of a wait: try_wait, which may suspend inside the instruction
+// until the phase completes; under a failure-path test bound (below
+// SHORT_WAIT_NS) the non-blocking test, so that a phase still pending at the
+// first probe always reaches the bound check.
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity, const WaitCtl &w)
+{
+    return w.limit_ns >= SHORT_WAIT_NS ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity);
+}
+
 // Single-thread bounded wait on phase `parity` of an mbarrier.  Returns false
 // when the limit ran out (the error word is set) or another thread gave up.
 __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtl &w)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_probe(bar, parity, w)) return true;
     return wait1_slow(bar, parity, w);
 }
 
@@ -601,7 +610,7 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitC
 // never diverge).
 __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const WaitCtl &w)
 {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__all_sync(0xffffffffu, mbar_probe(bar, parity, w))) return true;
     return waitw_slow(bar, parity, w);
 }
 
