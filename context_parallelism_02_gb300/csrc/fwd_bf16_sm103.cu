@@ -218,6 +218,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         x.n = SPLIT ? (int)((int64_t)n_all * (x.sp + 1) / so.n) - x.j0 : n_all;
         return x;
     };
+    // The block's next item with at least one key tile, from item_of(it) on:
+    // advances it and returns false once the block's items are used up.
+    auto next_busy = [&](int &it, Item &x) -> bool {
+        for (;; ++it) {
+            if (!PERSIST && it > 0) return false;
+            const int item = item_of(it);
+            if (item >= n_items) return false;
+            x = decode(item);
+            if (x.n > 0) return true;
+        }
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_Q), 1);
@@ -258,22 +269,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // ------------------------------------------------------------ producer
             const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
             int nq = 0, nk = 0, nv = 0;   // Q loads, K tiles, V halves issued so far
-            bool ok = true;
-            for (int it = 0; ok && (PERSIST || it == 0); ++it) {
-                const int item = item_of(it);
-                if (item >= n_items) break;
-                const Item x = decode(item);
-                if (x.n == 0) continue;
-                // the previous unit's S MMAs must be done with the single Q buffer
-                if (nq > 0 && !wait1(BAR(B_QEMPTY), (nq - 1) & 1, wc)) break;
+            // Q of item y into the single Q buffer, once the previous unit's S
+            // MMAs are done with it
+            auto load_q = [&](const Item &y) -> bool {
+                if (nq > 0 && !wait1(BAR(B_QEMPTY), (nq - 1) & 1, wc)) return false;
                 mbar_arrive_expect_tx(BAR(B_Q), C::QBYTES);
                 // map coordinates (rank, row) of the unit's first query
-                const int qmr = dbg_coord(a.err, STEP ? 0 : slot_mrank(g, x.w.q0), map_r);
-                const int qmw = dbg_coord(a.err, STEP ? slot_lrow(g, x.w.r, x.w.q0) : slot_mrow(g, x.w.q0), map_rows);
-                const int qh = dbg_coord(a.err, x.w.h, a.Hq), qb = dbg_coord(a.err, x.w.b, a.B);
+                const int qmr = dbg_coord(a.err, STEP ? 0 : slot_mrank(g, y.w.q0), map_r);
+                const int qmw = dbg_coord(a.err, STEP ? slot_lrow(g, y.w.r, y.w.q0) : slot_mrow(g, y.w.q0), map_rows);
+                const int qh = dbg_coord(a.err, y.w.h, a.Hq), qb = dbg_coord(a.err, y.w.b, a.B);
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load5(sQ + bx * 16384, &tmQ, BAR(B_Q), bx * 64, qh, qmr, qmw, qb, pol_q);
                 ++nq;
+                return true;
+            };
+            // Items with keys only, decoded one ahead while the current one loads;
+            // the next unit's Q goes out between the current unit's last K and
+            // last V (its S MMAs are done by then), so that the next unit's first
+            // S can run while the softmax warps finish this unit's epilogue.
+            int it = 0;
+            Item x;
+            bool have = next_busy(it, x);
+            bool ok = !have || load_q(x);
+            while (ok && have) {
+                int it2 = it + 1;
+                Item y = x;
                 // K runs one tile ahead of V; the V loads reuse the K tile starts
                 KvIter<KT> itk;
                 if (STEP)
@@ -282,7 +302,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     itk.begin(g, x.w.r, x.w.qmax);
                 if (SPLIT) itk.skip(x.j0);
                 int kr_cur = 0, kw_cur = 0, kr_next = 0, kw_next = 0;   // map coordinates (rank, row)
-                const int kvh = dbg_coord(a.err, x.kvh, a.Hkv);
+                const int kvh = dbg_coord(a.err, x.kvh, a.Hkv), qb = dbg_coord(a.err, x.w.b, a.B);
                 auto load_k = [&]() -> bool {   // the next K tile, global index nk
                     const int st = nk & 1;
                     if (nk >= 2 && !wait1(BAR(B_KEMPTY + st), ((nk >> 1) - 1) & 1, wc)) return false;
@@ -297,12 +317,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     return true;
                 };
                 ok = load_k();
+                const bool have2 = PERSIST && next_busy(it2, y);
                 for (int j = 0; ok && j < x.n; ++j) {
                     kr_cur = kr_next;
                     kw_cur = kw_next;
                     // global index of tile j: nv / 2 (V halves are issued tile by tile)
                     const int t = nv >> 1;
-                    if (j + 1 < x.n && !load_k()) {
+                    if ((j + 1 < x.n && !load_k()) || (j + 1 == x.n && have2 && !load_q(y))) {
                         ok = false;
                         break;
                     }
@@ -318,6 +339,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         ++nv;
                     }
                 }
+                x = y;
+                it = it2;
+                have = have2;
             }
             {
                 // Drain: wait (bounded) for the copies still in flight -- always,
@@ -328,7 +352,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 WaitCtl dc{a.err, &no_abort, a.drain_ns};
                 if (nq > 0) wait1(BAR(B_Q), (nq - 1) & 1, dc);
                 for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) wait1(BAR(B_KFULL + (j & 1)), (j >> 1) & 1, dc);
-                for (int x = nv > 2 ? nv - 2 : 0; x < nv; ++x) wait1(BAR(B_VFULL + (x & 1)), (x >> 1) & 1, dc);
+                for (int h = nv > 2 ? nv - 2 : 0; h < nv; ++h) wait1(BAR(B_VFULL + (h & 1)), (h >> 1) & 1, dc);
             }
         } else if (warp == 1 || warp == 2) {
             // ------------------------------------------------------------ MMA issuers
@@ -445,10 +469,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bool ok = true;
         int nu = 0, nt = 0, nx = 0;   // units finished, tiles done, row-max exchanges so far
 
-        for (int it = 0; ok && (PERSIST || it == 0); ++it) {
-            const int item = item_of(it);
-            if (item >= n_items) break;
-            const Item x = decode(item);
+        // Every item, empty ones included, decoded one ahead: the next one is
+        // decoded while this unit's last PV completes.
+        Item xn;
+        bool have = item_of(0) < n_items;
+        if (have) xn = decode(item_of(0));
+        auto advance = [&](int it) {
+            const int nxt = item_of(it + 1);
+            have = PERSIST && nxt < n_items;
+            if (have) xn = decode(nxt);
+        };
+        for (int it = 0; ok && have; ++it) {
+            const Item x = xn;
             const Unit &w = x.w;
             const int n = x.n;
             const int qpos = w.q0 + row;
@@ -491,6 +523,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             stp.lse_acc[((int64_t)w.b * a.Hq + w.h) * C_loc + lr] = NEG_INF;
                     }
                 }
+                advance(it);
                 continue;
             }
             float m_run = NEG_INF, l_run = 0.f;      // l_run: this half's share of the row sum
@@ -628,6 +661,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_PFULL));
             }
+            advance(it);
             if (!ok || !waitw(BAR(B_OFIN), nu & 1, wc)) {
                 ok = false;
                 break;
@@ -738,21 +772,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             } else {
                 __nv_bfloat16 *orow =
                     out + (((int64_t)w.b * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h) * D + (D / 2) * half;
+                // this half of the row: one tensor-memory load, rounded to bf16
+                uint32_t o[D / 2];
+                if constexpr (D == 128)
+                    tmem_ld_x64(tO, o);
+                else
+                    tmem_ld_x32(tO, o);
+                if (valid) {
+                    uint32_t pk[D / 4];
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tO + 32u * c, o);
-                    if (valid) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+                    for (int e = 0; e < D / 4; ++e)
+                        pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    // Every lane writes its own row (rows lie Hq*D elements apart), so
+                    // each store instruction touches 32 lines: whole 32-byte sectors
+                    // when the output allows it, else 16-byte pieces.
+                    if ((reinterpret_cast<uintptr_t>(out) & 31) == 0) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 pkt;
-                            pkt.x = pack_bf16(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-                            pkt.y = pack_bf16(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-                            pkt.z = pack_bf16(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-                            pkt.w = pack_bf16(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                            dst[v4] = pkt;
-                        }
+                        for (int c8 = 0; c8 < D / 32; ++c8)   // D/2 columns, 16 per store
+                            st_global_v8(orow + 16 * c8, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8 * c8));
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+                        for (int v4 = 0; v4 < D / 16; ++v4)   // D/2 columns, 8 per store
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                     }
                 }
                 if (valid && half == 0)

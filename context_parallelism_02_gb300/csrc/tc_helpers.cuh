@@ -101,6 +101,16 @@ __device__ __forceinline__ bool elect_one()
     return pred != 0;
 }
 
+// One 32-byte global store (eight 32-bit words); the address must be 32-byte
+// aligned.  A lane writes a whole sector, half the store instructions of
+// 16-byte stores.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
