@@ -274,6 +274,23 @@ struct Unit {
     int qmax;   // last valid query slot
 };
 
+// Chunk cu (in selected_chunk order) and position index pu of the i-th of the
+// nch * upc units of one (batch, head), numbered longest first: contiguous and
+// zigzag chunk by chunk (a unit's work grows with its chunk's position, and
+// within a chunk with its own), striped position by position over the chunks
+// (every rank's chunk has the same work profile, which grows with the local
+// position).
+CP_HD void unit_chunk_pos(const Geom &g, int nch, int upc, int i, int &cu, int &pu)
+{
+    if (striped(g)) {
+        cu = i % nch;
+        pu = i / nch;
+    } else {
+        pu = i % upc;
+        cu = i / upc;
+    }
+}
+
 CP_HD Unit decode_unit(const Geom &g, int B, int Hq, int lo, int hi, int upc, int qrows, int u)
 {
     Unit w;
@@ -281,8 +298,8 @@ CP_HD Unit decode_unit(const Geom &g, int B, int Hq, int lo, int hi, int upc, in
     int rest = u / Hq;
     w.b = rest % B;
     rest /= B;
-    int pu = rest % upc;
-    int cu = rest / upc;
+    int cu, pu;
+    unit_chunk_pos(g, num_selected_chunks(g, lo, hi), upc, rest, cu, pu);
     int ch = selected_chunk(g, lo, hi, cu);
     w.r = chunk_rank(g, ch);
     int cstart = ch * g.clen;
@@ -301,10 +318,9 @@ CP_HD Unit decode_unit_grouped(const Geom &g, int B, int Hq, int upc, int qrows,
 {
     const int nch = num_selected_chunks(g, 0, g.N);
     Unit w;
-    const int pu = u % upc;
-    int rest = u / upc;
-    const int cu = rest % nch;
-    rest /= nch;
+    int cu, pu;
+    unit_chunk_pos(g, nch, upc, u % (nch * upc), cu, pu);
+    const int rest = u / (nch * upc);
     w.h = rest % Hq;
     w.b = rest / Hq;
     const int ch = selected_chunk(g, 0, g.N, cu);

@@ -849,11 +849,13 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
     // every head's K/V at once; when those exceed what L2 can keep
     // (S = 131072: 512 MB), every query tile re-reads its K/V from DRAM, so a
     // launch over all ranks numbers each (batch, head) contiguously instead
-    // (blocks in flight share one or two heads' K/V).  Below ~48 MB of K/V the
-    // longest-first order costs no DRAM traffic and shortens the tail.
+    // (blocks in flight share one or two heads' K/V).  Up to 96 MB of K/V
+    // (of the 129 MB L2) the longest-first order was measured to cost no DRAM
+    // time and shortens the tail (S = 16384 and 20480, 67 and 84 MB of K/V:
+    // 16-19 % faster than the grouped order).
     const int64_t kv_bytes = 2ll * a.B * a.S * a.Hkv * D * 2;
     a.head_grouped = (MODE != MODE_STEP && a.rank_lo == 0 && a.rank_hi == a.N &&
-                      kv_bytes > 48ll * 1024 * 1024) ? 1 : 0;
+                      kv_bytes > 96ll * 1024 * 1024) ? 1 : 0;
     const int64_t units = (int64_t)num_selected_chunks(g, a.rank_lo, a.rank_hi) * a.upc * a.B * a.Hq;
     if (units == 0) return CP_OK;
     const int64_t items = units * (MODE == MODE_SPLIT ? so.n : 1);
@@ -864,12 +866,14 @@ int launch_d(const void *q, const void *k, const void *v, void *out, float *lse,
     // fixed cost of a block (barrier set-up, tensor-memory allocation, the Q load
     // and the pipeline fill before the first PV, the epilogue) weighs, so one
     // persistent block per SM runs several items, loading the next unit's Q
-    // while the previous one finishes.
-    // (A split launch already spreads long rows over blocks; it keeps one
-    // block per item.)
+    // while the previous one finishes.  Its static assignment (alternating
+    // rounds over the numbering) balances only a longest-first numbering, so a
+    // head-grouped launch keeps one block per item and the hardware's dynamic
+    // dispatch.  (A split launch already spreads long rows over blocks; it
+    // keeps one block per item too.)
     int64_t blocks = items;
     const int64_t sms = sm_count();
-    if (MODE != MODE_SPLIT && items <= 16 * sms && items > sms) blocks = sms;
+    if (MODE != MODE_SPLIT && !a.head_grouped && items <= 16 * sms && items > sms) blocks = sms;
     const int cap = fwd_grid_limit();   // test hook: the grid, overriding the rule above
     if (cap > 0) blocks = items < cap ? items : cap;
     const float sl2 = a.scale * 1.4426950408889634f;

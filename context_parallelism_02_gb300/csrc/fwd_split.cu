@@ -162,15 +162,9 @@ int fwd_split_choose(int B, int Hq, int S, int D, int N, int causal, int layout,
         double makespan = 0.0;
         for (int sp = 0; sp < ns; ++sp)   // blocks in launch order: split index slowest
             for (int64_t u = 0; u < units; ++u) {
-                int64_t pu, cu;
-                if (grouped) {
-                    pu = u % upc;
-                    cu = (u / upc) % nch;
-                } else {
-                    const int64_t r = u / ((int64_t)B * Hq);
-                    pu = r % upc;
-                    cu = r / upc;
-                }
+                int cu, pu;
+                unit_chunk_pos(g, nch, upc, (int)(grouped ? u % ((int64_t)nch * upc) : u / ((int64_t)B * Hq)), cu,
+                               pu);
                 const int64_t n = tiles[(size_t)(cu * upc + pu)];
                 const int64_t len = n * (sp + 1) / ns - n * sp / ns;
                 const double t =

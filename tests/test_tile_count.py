@@ -1,5 +1,6 @@
-"""Host logic of the ring kernels' tile walk (no GPU): the closed-form count
-over the whole ring, the per-step counts and the walk itself agree."""
+"""Host logic of the ring kernels' work decomposition (no GPU): the
+closed-form tile count over the whole ring, the per-step counts and the walk
+itself agree, and both unit numberings cover every query tile exactly once."""
 import os
 import shutil
 import subprocess
