@@ -64,9 +64,10 @@ constexpr int QT = 128;          // query rows per unit
 constexpr int KT = 256;          // keys per KV tile
 constexpr int NTHREADS = 384;
 // Register split (setmaxnreg): the block launches at 168 registers per thread
-// (64512 in total); warpgroup 0 drops to 56 and the two softmax warpgroups
-// rise to 208: 128*56 + 256*208 = 60416.
-constexpr int REGS_CTRL = 56;
+// (64512 in total); warpgroup 0 drops to 64 and the two softmax warpgroups
+// rise to 208: 128*64 + 256*208 = 61440.  (At 56 the persistent control
+// warps spilled.)
+constexpr int REGS_CTRL = 64;
 constexpr int REGS_SOFTMAX = 208;
 static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= NTHREADS * 168, "register split exceeds the launch budget");
 constexpr float RESCALE_LOG2 = 8.0f;   // rescale O only when the max grows by > 2^8
@@ -716,35 +717,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 float *orow = stp.out_acc + srow * D + (D / 2) * half;
                 __nv_bfloat16 *frow = static_cast<__nv_bfloat16 *>(stp.out_final) + srow * D + (D / 2) * half;
+                // this half of the row: one tensor-memory load
+                uint32_t o[D / 2];
+                if constexpr (D == 128)
+                    tmem_ld_x64(tO, o);
+                else
+                    tmem_ld_x32(tO, o);
+                if (valid) {
+                    // 16 columns at a time: the state in 32-byte pieces when both
+                    // buffers allow it (each lane reads and writes its own row), else
+                    // 16-byte pieces
+                    const bool a32 = ((reinterpret_cast<uintptr_t>(stp.out_acc) |
+                                       reinterpret_cast<uintptr_t>(stp.out_final)) & 31) == 0;
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tO + 32u * c, o);
-                    if (valid) {
-                        float4 *dst = reinterpret_cast<float4 *>(orow + 32 * c);
-                        uint4 *fdst = reinterpret_cast<uint4 *>(frow + 32 * c);
-                        // 8 columns at a time: two float4 of state, one uint4 of bf16
+                    for (int c16 = 0; c16 < D / 32; ++c16) {   // D/2 columns
+                        float pv[16], r[16];
+                        float *src = orow + 16 * c16;
+                        if (stp.accumulate) {
+                            if (a32) {
+                                ld_global_v8f(src, pv);
+                                ld_global_v8f(src + 8, pv + 8);
+                            } else {
 #pragma unroll
-                        for (int v8 = 0; v8 < 4; ++v8) {
-                            float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
-                            if (stp.accumulate) {
-                                p0 = dst[2 * v8];
-                                p1 = dst[2 * v8 + 1];
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    const float4 t = reinterpret_cast<const float4 *>(src)[q4];
+                                    pv[4 * q4] = t.x;
+                                    pv[4 * q4 + 1] = t.y;
+                                    pv[4 * q4 + 2] = t.z;
+                                    pv[4 * q4 + 3] = t.w;
+                                }
                             }
-                            const uint32_t *ov = o + 8 * v8;
-                            const float4 r0 = make_float4(wa * p0.x + wb * __uint_as_float(ov[0]),
-                                                          wa * p0.y + wb * __uint_as_float(ov[1]),
-                                                          wa * p0.z + wb * __uint_as_float(ov[2]),
-                                                          wa * p0.w + wb * __uint_as_float(ov[3]));
-                            const float4 r1 = make_float4(wa * p1.x + wb * __uint_as_float(ov[4]),
-                                                          wa * p1.y + wb * __uint_as_float(ov[5]),
-                                                          wa * p1.z + wb * __uint_as_float(ov[6]),
-                                                          wa * p1.w + wb * __uint_as_float(ov[7]));
-                            dst[2 * v8] = r0;
-                            dst[2 * v8 + 1] = r1;
-                            if (stp.out_final)
-                                fdst[v8] = make_uint4(pack_bf16(r0.x, r0.y), pack_bf16(r0.z, r0.w),
-                                                      pack_bf16(r1.x, r1.y), pack_bf16(r1.z, r1.w));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) pv[e] = 0.f;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r[e] = wa * pv[e] + wb * __uint_as_float(o[16 * c16 + e]);
+                        if (a32) {
+                            st_global_v8f(src, r);
+                            st_global_v8f(src + 8, r + 8);
+                        } else {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                reinterpret_cast<float4 *>(src)[q4] =
+                                    make_float4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
+                        }
+                        if (stp.out_final) {
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(r[2 * e], r[2 * e + 1]);
+                            if (a32) {
+                                st_global_v8(frow + 16 * c16, pk);
+                            } else {
+                                uint4 *fdst = reinterpret_cast<uint4 *>(frow + 16 * c16);
+                                fdst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                                fdst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                            }
                         }
                     }
                 }
