@@ -783,16 +783,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int64_t prow =
                     (((int64_t)x.sp * a.B + w.b) * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h;
                 float *orow = so.out + prow * D + (D / 2) * half;
+                // this half of the row: one tensor-memory load, written in 32-byte
+                // pieces when the partials allow it, else 16-byte pieces
+                uint32_t o[D / 2];
+                if constexpr (D == 128)
+                    tmem_ld_x64(tO, o);
+                else
+                    tmem_ld_x32(tO, o);
+                if (valid) {
+                    float r[D / 2];
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tO + 32u * c, o);
-                    if (valid) {
-                        float4 *dst = reinterpret_cast<float4 *>(orow + 32 * c);
+                    for (int e = 0; e < D / 2; ++e) r[e] = __uint_as_float(o[e]) * inv;
+                    if ((reinterpret_cast<uintptr_t>(so.out) & 31) == 0) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
-                                                  __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+                        for (int c8 = 0; c8 < D / 16; ++c8) st_global_v8f(orow + 8 * c8, r + 8 * c8);   // D/2 columns
+                    } else {
+#pragma unroll
+                        for (int v4 = 0; v4 < D / 8; ++v4)   // D/2 columns, 4 per store
+                            reinterpret_cast<float4 *>(orow)[v4] =
+                                make_float4(r[4 * v4], r[4 * v4 + 1], r[4 * v4 + 2], r[4 * v4 + 3]);
                     }
                 }
                 if (valid && half == 0)
