@@ -524,9 +524,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // warpgroup s%2 turns them into P^T and dS^T (bf16 pairs, written over the
 // first half of the columns it read); then dV += P^T dO_s and dK += dS^T Q_s
 // (N=D, K=64).  With two buffers and one warpgroup per buffer, the MMAs of
-// step s+1 run while warpgroup s%2 works on step s; S^T/dP^T(s+2) is issued
-// into buffer s%2 once dV/dK(s) has completed (a commit barrier, since the two
-// MMA groups come from different issuing threads).
+// step s+1 run while warpgroup s%2 works on step s.  S^T and dP^T have
+// barriers of their own: S^T(s+2) is issued into buffer s%2 once dV(s) has
+// read P^T(s) out of the S^T columns, dP^T(s+2) once dK(s) has read dS^T(s)
+// out of the dP^T columns (commit barriers, since the MMA groups come from
+// different issuing warps), and the gradient warps turn S^T into P^T before
+// they wait for dP^T.  A buffer's serial chain is then P^T -> dV -> S^T of
+// the step after next, without the dS^T and dK stages.
 // Each gradient thread handles all 64 columns of its steps, so it moves them
 // with two 64-column tensor-memory loads and two 32-column stores.
 //
@@ -539,13 +543,15 @@ enum {
     K_KVFULL = 0,
     K_QFULL = 1,                  // K_QST half stages
     K_QEMPTY = 1 + K_QST,         // K_QST half stages
-    K_SDP = 1 + 2 * K_QST,        // 2 buffers: S^T, dP^T complete
+    K_S = 1 + 2 * K_QST,          // 2 buffers: S^T complete
     K_PW = 3 + 2 * K_QST,         // 2 buffers: P^T written (4 arrivals: one warpgroup)
-    K_BUF = 5 + 2 * K_QST,        // 2 buffers: dV/dK(s) complete, buffer s%2 may be rewritten
+    K_SFREE = 5 + 2 * K_QST,      // 2 buffers: dV(s) complete, the S^T columns may be rewritten
     K_FIN = 7 + 2 * K_QST,
-    K_DRAIN = 8 + 2 * K_QST,      // one commit per issuing thread (2)
+    K_DRAIN = 8 + 2 * K_QST,      // one commit per issuing warp (3)
     K_DSW = 9 + 2 * K_QST,        // 2 buffers: dS^T written (4 arrivals)
-    K_NBAR = 11 + 2 * K_QST
+    K_DP = 11 + 2 * K_QST,        // 2 buffers: dP^T complete
+    K_DPFREE = 13 + 2 * K_QST,    // 2 buffers: dK(s) complete, the dP^T columns may be rewritten
+    K_NBAR = 15 + 2 * K_QST
 };
 
 template <int D>
@@ -603,13 +609,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(BAR(K_QEMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(BAR(K_SDP + i), 1);
+            mbar_init(BAR(K_S + i), 1);
+            mbar_init(BAR(K_DP + i), 1);
             mbar_init(BAR(K_PW + i), 4);
             mbar_init(BAR(K_DSW + i), 4);
-            mbar_init(BAR(K_BUF + i), 1);
+            mbar_init(BAR(K_SFREE + i), 1);
+            mbar_init(BAR(K_DPFREE + i), 1);
         }
         mbar_init(BAR(K_FIN), 1);
-        mbar_init(BAR(K_DRAIN), 2);
+        mbar_init(BAR(K_DRAIN), 3);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -689,32 +697,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int s = issued > K_QST ? issued - K_QST : 0; s < issued; ++s)
                     wait1(BAR(K_QFULL + s % K_QST), (s / K_QST) & 1, dc);
             }
-        } else if (warp == 1 || warp == 2) {
+        } else {
             // ------------------------------------------------------------ MMA issuers
-            // Two issuing warps, so that a wait of one never leaves the tensor
-            // pipe without work from the other: warp 2 issues S^T/dP^T(s) into
-            // buffer s%2 once dV/dK(s-2) has finished reading it; warp 1 issues
-            // dV/dK(s) once the gradient warpgroup has written P^T(s) and dS^T(s).
-            // Each warp runs converged (warp-collective waits), so its operands
-            // stay warp-uniform, and one elected lane issues the MMAs and commits.
+            // Three issuing warps, so that a wait of one never leaves the tensor
+            // pipe without work from the others: warp 2 issues S^T(s) into buffer
+            // s%2 once dV(s-2) has read P^T(s-2) out of those columns, warp 3
+            // dP^T(s) once dK(s-2) has read dS^T(s-2), and warp 1 dV(s) and dK(s)
+            // once the gradient warpgroup has written P^T(s) and dS^T(s).  Each
+            // warp runs converged (warp-collective waits), so its operands stay
+            // warp-uniform, and one elected lane issues the MMAs and commits.
             const bool leader = elect_one();
             bool ok = waitw(BAR(K_KVFULL), 0, wc);
-            if (warp == 2) {
+            if (warp >= 2) {
                 constexpr uint32_t idSP = idesc_bf16(128, 64, false);   // N = 64 queries
-                const uint64_t dKd = sdesc(sK, 16, 1024), dVd = sdesc(sV, 16, 1024);
-                const uint64_t dQ0 = sdesc(sQ, 16, 1024);               // Q_s K-major (64-row boxes)
+                // warp 2: S^T = K Q_s^T; warp 3: dP^T = V dO_s^T
+                const bool dp = warp == 3;
+                const uint64_t dA = sdesc(dp ? sV : sK, 16, 1024);
+                const uint64_t dQ0 = sdesc(sQ, 16, 1024) + (dp ? (uint64_t)(HB >> 4) : 0);   // Q_s / dO_s K-major
+                const int b_free = dp ? K_DPFREE : K_SFREE, b_done = dp ? K_DP : K_S;
+                const uint32_t col = dp ? 64u : 0u;
                 Ring<K_QST> rs;
                 for (int s = 0; ok && s < ns; ++s, rs.next()) {
-                    if ((s >= 2 && !waitw(BAR(K_BUF + (s & 1)), ((s >> 1) - 1) & 1, wc)) ||
+                    if ((s >= 2 && !waitw(BAR(b_free + (s & 1)), ((s >> 1) - 1) & 1, wc)) ||
                         !waitw(BAR(K_QFULL + rs.st), rs.ph, wc))
                         break;
-                    const uint32_t tb = tmem + 128u * (uint32_t)(s & 1);
+                    const uint32_t tb = tmem + 128u * (uint32_t)(s & 1) + col;
                     const uint64_t so = (uint64_t)(rs.st * (C::STAGE >> 4));
                     if (leader) {
                         tc_fence_after();
-                        ss_seq<0, D, 8192>(tb, dKd, dQ0 + so, idSP);
-                        ss_seq<0, D, 8192>(tb + 64u, dVd, dQ0 + so + (uint64_t)(HB >> 4), idSP);
-                        mma_commit(BAR(K_SDP + (s & 1)));
+                        ss_seq<0, D, 8192>(tb, dA, dQ0 + so, idSP);
+                        mma_commit(BAR(b_done + (s & 1)));
                     }
                     __syncwarp();
                 }
@@ -733,16 +745,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (leader) {
                         tc_fence_after();
                         ts_mn_seq<0, 4, 0>(tDV, tb, dQmn0 + so + (uint64_t)(HB >> 4), idKV, acc0);
+                        mma_commit(BAR(K_SFREE + (s & 1)));
                     }
                     __syncwarp();
                     if (!waitw(BAR(K_DSW + (s & 1)), (s >> 1) & 1, wc)) break;
                     if (leader) {
                         tc_fence_after();
                         ts_mn_seq<0, 4, 0>(tDK, tb + 64u, dQmn0 + so, idKV, acc0);
-                        // S^T/dP^T(s) completed before the gradient warps started, so the
-                        // stage is free once dV/dK(s) completes
+                        // S^T(s) and dP^T(s) completed before the gradient warps read
+                        // them, so the stage is free once dV/dK(s) complete
                         mma_commit(BAR(K_QEMPTY + rs.st));
-                        mma_commit(BAR(K_BUF + (s & 1)));
+                        mma_commit(BAR(K_DPFREE + (s & 1)));
                     }
                     __syncwarp();
                 }
@@ -780,13 +793,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (half) qr.next();
         for (int i = 0; 2 * i + half < ns; ++i, it.next(), qr.next(), qr.next()) {
             const int qa = it.start() + 64 * half, ql = it.len() - 64 * half, sh = it.shift;
-            if (!waitw(BAR(K_SDP + half), i & 1, wc) || !waitw(BAR(K_QFULL + qr.st), qr.ph, wc)) {
+            if (!waitw(BAR(K_S + half), i & 1, wc) || !waitw(BAR(K_QFULL + qr.st), qr.ph, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t sr[64], pr[64];
-            tmem_ld2_x64(tb, sr, tb + 64u, pr);
+            tmem_ld_x64(tb, sr);
             // visible query columns c: c < ql and (not causal or qa + c >= kpos)
             const int lo = a.causal ? kpos - sh - qa : 0;
             const float4 *ls4 = reinterpret_cast<const float4 *>(stat + qr.st * 128);   // -lse2
@@ -827,6 +840,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(K_PW + half));   // dV(s) may start
             }
+            if (!waitw(BAR(K_DP + half), i & 1, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_ld_x64(tb + 64u, pr);
             {
                 // dS^T = P^T (dP^T - Delta)
                 uint32_t dd[32];
