@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // dV [256, 256+D), dK [256+D, 256+2D).  Shared memory: K and V (128 rows),
 // K_QST half stages of (Q_s, dO_s) 64-row tiles, and their lse / Delta.
 
-constexpr int K_QST = 4;
+constexpr int K_QST = 5;
 enum {
     K_KVFULL = 0,
     K_QFULL = 1,                  // K_QST half stages
