@@ -868,9 +868,11 @@ def main():
         e2e_all.append(t0.elapsed_time(t1) / e2e_steps)
     e2e_clocks = e2e_sampler.stop()
     # what the copies do to the forward: one forward with the next step's whole
-    # upload running beside it on the copy stream, against the same forward
-    # and the upload alone (CUDA events; medians of three)
-    conc = {"fwd_alone": [], "fwd_with_upload": [], "upload_alone": []}
+    # upload running beside it on the copy stream, with the upload and a
+    # read-back of the previous outputs beside it (both directions, as in the
+    # pipelined steps), against the same forward and the upload alone (CUDA
+    # events; medians of three)
+    conc = {"fwd_alone": [], "fwd_with_upload": [], "upload_alone": [], "fwd_with_upload_and_readback": []}
     for _ in range(3):
         for key in conc:
             torch.cuda.synchronize()
@@ -878,12 +880,18 @@ def main():
             a1 = torch.cuda.Event(enable_timing=True)
             a0.record(stream)
             up.wait_event(a0)
+            down.wait_event(a0)
             if key != "upload_alone":
                 step()
             if key != "fwd_alone":
                 with torch.cuda.stream(up):
                     upload(1)
+            if key == "fwd_with_upload_and_readback":
+                with torch.cuda.stream(down):
+                    for h_, d_ in zip(outs_h[1], outs[1]):
+                        h_.copy_(d_, non_blocking=True)
             stream.wait_stream(up)
+            stream.wait_stream(down)
             a1.record(stream)
             torch.cuda.synchronize()
             conc[key].append(a0.elapsed_time(a1))
@@ -939,6 +947,7 @@ def main():
                 "copy_ms_per_step": h2d / link["h2d"] / 1e6 + d2h / link["d2h"] / 1e6,
                 "fwd_alone_ms": statistics.median(conc["fwd_alone"]),
                 "fwd_with_concurrent_upload_ms": statistics.median(conc["fwd_with_upload"]),
+                "fwd_with_upload_and_readback_ms": statistics.median(conc["fwd_with_upload_and_readback"]),
                 "upload_alone_ms": statistics.median(conc["upload_alone"]),
                 "sm_mhz": e2e_clocks.get("sm_mhz"),
                 "power_w_max": e2e_clocks.get("power_w_max"),
