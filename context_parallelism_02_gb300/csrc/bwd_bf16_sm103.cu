@@ -26,10 +26,11 @@
 // is written once, and the result is deterministic.
 //
 // Roles of both tensor-core kernels (384 threads, three warpgroups): warp 0
-// TMA producer (dQ: K tiles; warp 3 loads Q, dO and V), warps 1 and 2 MMA
-// issuers (one thread each), warps 4-7 and 8-11 the elementwise gradient
-// (dQ: the two 64-column halves of one 128x128 tile; dK/dV: one warpgroup per
-// half-step buffer), one thread per tensor-memory lane.  Every wait is bounded.
+// TMA producer (dQ: K tiles; warp 3 loads Q, dO and V), MMA issuers that run
+// converged with one elected lane issuing (dQ: warps 1 and 2; dK/dV: warps 1,
+// 2 and 3), warps 4-7 and 8-11 the elementwise gradient (dQ: the two
+// 64-column halves of one 128x128 tile; dK/dV: one warpgroup per half-step
+// buffer), one thread per tensor-memory lane.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -25,11 +25,12 @@
 // items in turn, with every barrier phase a running count across items.
 //
 // Roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: Q once; K tiles (256 rows) into a 2-deep ring
-//               one tile ahead; V tiles as two 128-row halves; also allocates
-//               and frees the 512 tensor-memory columns.
-//   warp 1      issues S = Q K^T (one thread).
-//   warp 2      issues O += P V (one thread).
+//   warp 0      TMA producer (one thread): Q once per unit (the next unit's
+//               Q before the current unit's last V); K tiles (256 rows) into
+//               a 2-deep ring one tile ahead; V tiles as two 128-row halves;
+//               warp 0 also allocates and frees the 512 tensor-memory columns.
+//   warp 1      issues S = Q K^T, warp 2 issues O += P V: each runs converged
+//               (warp-collective waits) and one elected lane issues.
 //   warp 3      idle (it completes warpgroup 0 for the register split).
 //   warps 4-7   softmax of key columns [0,128), warps 8-11 of [128,256):
 //               one thread per query row.  The halves exchange row maxima
