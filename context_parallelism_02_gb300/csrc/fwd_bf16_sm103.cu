@@ -135,54 +135,6 @@ __device__ __forceinline__ void issue_pv_seq(uint32_t tO, uint32_t tP, uint64_t 
     }
 }
 
-// --- output stores ---------------------------------------------------------------
-
-// Writes the warp's 32 half-rows of bf16 output (lane t holds row t's NW words of
-// bf16 pairs; rows anywhere in memory, 32-byte aligned) so that every store
-// instruction covers whole half-rows.  A lane storing its own row would make each
-// instruction touch 32 lines; here lanes in groups of G = NW/8 swap 32-byte
-// chunks over shuffles, and lane j of a group then stores chunk j of each of the
-// group's G rows, one row per instruction.  Every lane of the warp calls it; rows
-// with ok == false are not written.
-template <int NW>
-__device__ __forceinline__ void store_half_rows(__nv_bfloat16 *row, bool ok, const uint32_t (&pk)[NW], int lane)
-{
-    constexpr int G = NW / 8;
-    static_assert(G == 2 || G == 4, "half-rows of 64 or 128 bytes");
-    const int j = lane & (G - 1), gb = lane & ~(G - 1);
-    // rv[k]: chunk j of the row of lane gb + (j ^ k); in exchange k this lane sends
-    // its chunk j ^ k, the one that lane wants
-    uint32_t rv[G][8];
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-        const int c = j ^ k;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            uint32_t v = pk[e];
-#pragma unroll
-            for (int cc = 1; cc < G; ++cc) v = c == cc ? pk[8 * cc + e] : v;
-            rv[k][e] = k == 0 ? v : __shfl_xor_sync(0xffffffffu, v, k);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < G; ++m) {   // instruction m: the row of lane gb + m
-        const int k = j ^ m;
-        uint32_t d[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            uint32_t v = rv[0][e];
-#pragma unroll
-            for (int kk = 1; kk < G; ++kk) v = k == kk ? rv[kk][e] : v;
-            d[e] = v;
-        }
-        const int src = gb + m;
-        const bool rok = __shfl_sync(0xffffffffu, ok ? 1 : 0, src) != 0;
-        __nv_bfloat16 *rp = reinterpret_cast<__nv_bfloat16 *>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(row), src));
-        if (rok) st_global_v8(rp + 16 * j, d);
-    }
-}
-
 // --- the kernel ------------------------------------------------------------------
 
 // Modes:
@@ -870,10 +822,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
                 // Rows lie Hq*D elements apart.  With a 32-byte aligned output the
                 // warp regroups its half-rows so that each store instruction writes
-                // whole ones (store_half_rows); otherwise every lane writes its own
+                // whole ones (store_warp_rows); otherwise every lane writes its own
                 // row in 16-byte pieces.
                 if ((reinterpret_cast<uintptr_t>(out) & 31) == 0) {
-                    store_half_rows<D / 4>(orow, valid, pk, lane);
+                    store_warp_rows<D / 4>(orow, valid, pk, lane);
                 } else if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll

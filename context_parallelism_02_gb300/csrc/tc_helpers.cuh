@@ -111,6 +111,52 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8])
                  : "memory");
 }
 
+// Writes one piece of NW words (NW*4 = 64 or 128 bytes of bf16 pairs) per lane,
+// lane t's piece in its own row (rows anywhere in memory, pieces 32-byte
+// aligned), so that every store instruction covers whole pieces.  A lane storing
+// its own piece would make each instruction touch 32 lines; here lanes in groups
+// of G = NW/8 swap 32-byte chunks over shuffles, and lane j of a group then
+// stores chunk j of each of the group's G pieces, one piece per instruction.
+// Every lane of the warp calls it; pieces with ok == false are not written.
+template <int NW>
+__device__ __forceinline__ void store_warp_rows(void *piece, bool ok, const uint32_t (&pk)[NW], int lane)
+{
+    constexpr int G = NW / 8;
+    static_assert(G == 2 || G == 4, "pieces of 64 or 128 bytes");
+    const int j = lane & (G - 1), gb = lane & ~(G - 1);
+    // rv[k]: chunk j of the piece of lane gb + (j ^ k); in exchange k this lane
+    // sends its chunk j ^ k, the one that lane wants
+    uint32_t rv[G][8];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        const int c = j ^ k;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            uint32_t v = pk[e];
+#pragma unroll
+            for (int cc = 1; cc < G; ++cc) v = c == cc ? pk[8 * cc + e] : v;
+            rv[k][e] = k == 0 ? v : __shfl_xor_sync(0xffffffffu, v, k);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < G; ++m) {   // instruction m: the piece of lane gb + m
+        const int k = j ^ m;
+        uint32_t d[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            uint32_t v = rv[0][e];
+#pragma unroll
+            for (int kk = 1; kk < G; ++kk) v = k == kk ? rv[kk][e] : v;
+            d[e] = v;
+        }
+        const int src = gb + m;
+        const bool rok = __shfl_sync(0xffffffffu, ok ? 1 : 0, src) != 0;
+        uint8_t *rp = reinterpret_cast<uint8_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(piece), src));
+        if (rok) st_global_v8(rp + 32 * j, d);
+    }
+}
+
 // Eight fp32 values from / to global memory in one 32-byte access (32-byte
 // aligned addresses only).
 __device__ __forceinline__ void ld_global_v8f(const float *p, float *r)
