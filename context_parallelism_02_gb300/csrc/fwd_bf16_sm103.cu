@@ -724,29 +724,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tmem_ld_x64(tO, o);
                 else
                     tmem_ld_x32(tO, o);
-                if (valid) {
-                    // 16 columns at a time: the state in 32-byte pieces when both
-                    // buffers allow it (each lane reads and writes its own row), else
-                    // 16-byte pieces
-                    const bool a32 = ((reinterpret_cast<uintptr_t>(stp.out_acc) |
-                                       reinterpret_cast<uintptr_t>(stp.out_final)) & 31) == 0;
+                const bool a32 = ((reinterpret_cast<uintptr_t>(stp.out_acc) |
+                                   reinterpret_cast<uintptr_t>(stp.out_final)) & 31) == 0;
+                if (a32) {
+                    // The state in pieces of 32 columns (128 bytes of fp32), read and
+                    // written regrouped so that every load and store instruction of
+                    // the warp covers whole pieces (rows lie Hq*D elements apart);
+                    // out_final's half-row is written the same way.
+                    uint32_t fk[D / 4];
+#pragma unroll
+                    for (int pc = 0; pc < D / 64; ++pc) {
+                        uint32_t pv[32], r[32];
+                        if (stp.accumulate) {
+                            load_warp_rows<32>(orow + 32 * pc, valid, pv, lane);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) pv[e] = 0u;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(wa * __uint_as_float(pv[e]) + wb * __uint_as_float(o[32 * pc + e]));
+                        store_warp_rows<32>(orow + 32 * pc, valid, r, lane);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            fk[16 * pc + e] = pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                    }
+                    if (stp.out_final) store_warp_rows<D / 4>(frow, valid, fk, lane);
+                } else if (valid) {
+                    // every lane reads and writes its own row, 16 bytes at a time
 #pragma unroll
                     for (int c16 = 0; c16 < D / 32; ++c16) {   // D/2 columns
                         float pv[16], r[16];
                         float *src = orow + 16 * c16;
                         if (stp.accumulate) {
-                            if (a32) {
-                                ld_global_v8f(src, pv);
-                                ld_global_v8f(src + 8, pv + 8);
-                            } else {
 #pragma unroll
-                                for (int q4 = 0; q4 < 4; ++q4) {
-                                    const float4 t = reinterpret_cast<const float4 *>(src)[q4];
-                                    pv[4 * q4] = t.x;
-                                    pv[4 * q4 + 1] = t.y;
-                                    pv[4 * q4 + 2] = t.z;
-                                    pv[4 * q4 + 3] = t.w;
-                                }
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float4 t = reinterpret_cast<const float4 *>(src)[q4];
+                                pv[4 * q4] = t.x;
+                                pv[4 * q4 + 1] = t.y;
+                                pv[4 * q4 + 2] = t.z;
+                                pv[4 * q4 + 3] = t.w;
                             }
                         } else {
 #pragma unroll
@@ -754,26 +771,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
 #pragma unroll
                         for (int e = 0; e < 16; ++e) r[e] = wa * pv[e] + wb * __uint_as_float(o[16 * c16 + e]);
-                        if (a32) {
-                            st_global_v8f(src, r);
-                            st_global_v8f(src + 8, r + 8);
-                        } else {
 #pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4)
-                                reinterpret_cast<float4 *>(src)[q4] =
-                                    make_float4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
-                        }
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            reinterpret_cast<float4 *>(src)[q4] =
+                                make_float4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
                         if (stp.out_final) {
                             uint32_t pk[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(r[2 * e], r[2 * e + 1]);
-                            if (a32) {
-                                st_global_v8(frow + 16 * c16, pk);
-                            } else {
-                                uint4 *fdst = reinterpret_cast<uint4 *>(frow + 16 * c16);
-                                fdst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                                fdst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                            }
+                            uint4 *fdst = reinterpret_cast<uint4 *>(frow + 16 * c16);
+                            fdst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            fdst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                         }
                     }
                 }
@@ -784,26 +792,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int64_t prow =
                     (((int64_t)x.sp * a.B + w.b) * a.S + dbg_coord(a.err, valid ? qp : 0, a.S)) * a.Hq + w.h;
                 float *orow = so.out + prow * D + (D / 2) * half;
-                // this half of the row: one tensor-memory load, written in 32-byte
-                // pieces when the partials allow it, else 16-byte pieces
+                // this half of the row: one tensor-memory load; with 32-byte aligned
+                // partials written in pieces of 32 columns (128 bytes), regrouped so
+                // that every store instruction of the warp covers whole pieces,
+                // else every lane writes its own row in 16-byte pieces
                 uint32_t o[D / 2];
                 if constexpr (D == 128)
                     tmem_ld_x64(tO, o);
                 else
                     tmem_ld_x32(tO, o);
-                if (valid) {
-                    float r[D / 2];
 #pragma unroll
-                    for (int e = 0; e < D / 2; ++e) r[e] = __uint_as_float(o[e]) * inv;
-                    if ((reinterpret_cast<uintptr_t>(so.out) & 31) == 0) {
+                for (int e = 0; e < D / 2; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv);
+                if ((reinterpret_cast<uintptr_t>(so.out) & 31) == 0) {
 #pragma unroll
-                        for (int c8 = 0; c8 < D / 16; ++c8) st_global_v8f(orow + 8 * c8, r + 8 * c8);   // D/2 columns
-                    } else {
+                    for (int pc = 0; pc < D / 64; ++pc)
+                        store_warp_rows<32>(orow + 32 * pc, valid, *reinterpret_cast<const uint32_t(*)[32]>(o + 32 * pc),
+                                            lane);
+                } else if (valid) {
 #pragma unroll
-                        for (int v4 = 0; v4 < D / 8; ++v4)   // D/2 columns, 4 per store
-                            reinterpret_cast<float4 *>(orow)[v4] =
-                                make_float4(r[4 * v4], r[4 * v4 + 1], r[4 * v4 + 2], r[4 * v4 + 3]);
-                    }
+                    for (int v4 = 0; v4 < D / 8; ++v4)   // D/2 columns, 4 per store
+                        reinterpret_cast<float4 *>(orow)[v4] =
+                            make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
+                                        __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
                 }
                 if (valid && half == 0)
                     so.lse[prow] = l_tot > 0.f ? (m_run + lg2(l_tot)) * 0.69314718055994531f : NEG_INF;

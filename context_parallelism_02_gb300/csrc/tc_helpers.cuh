@@ -157,6 +157,60 @@ __device__ __forceinline__ void store_warp_rows(void *piece, bool ok, const uint
     }
 }
 
+// Eight 32-bit words from global memory in one 32-byte access (32-byte aligned).
+__device__ __forceinline__ void ld_global_v8u(const void *p, uint32_t (&v)[8])
+{
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "l"(p)
+                 : "memory");
+}
+
+// The load counterpart of store_warp_rows: lane t receives the NW words of its
+// own piece, and every load instruction of the warp covers whole pieces.  Lane j
+// of a group of G = NW/8 lanes loads chunk j of each of the group's G pieces,
+// one piece per instruction; the chunks then go to their pieces' lanes over
+// shuffles.  Every lane of the warp calls it; pieces with ok == false are not
+// read (their words come back 0).
+template <int NW>
+__device__ __forceinline__ void load_warp_rows(const void *piece, bool ok, uint32_t (&pk)[NW], int lane)
+{
+    constexpr int G = NW / 8;
+    static_assert(G == 2 || G == 4, "pieces of 64 or 128 bytes");
+    const int j = lane & (G - 1), gb = lane & ~(G - 1);
+    uint32_t ld[G][8];   // ld[m]: chunk j of the piece of lane gb + m
+#pragma unroll
+    for (int m = 0; m < G; ++m) {
+        const int src = gb + m;
+        const bool rok = __shfl_sync(0xffffffffu, ok ? 1 : 0, src) != 0;
+        const uint8_t *rp = reinterpret_cast<const uint8_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(piece), src));
+        if (rok) {
+            ld_global_v8u(rp + 32 * j, ld[m]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ld[m][e] = 0u;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < NW; ++e) pk[e] = 0u;
+    // exchange k: this lane sends chunk j of the piece of lane gb + (j ^ k), which
+    // that lane wants, and receives chunk j ^ k of its own piece
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        const int c = j ^ k;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            uint32_t v = ld[0][e];
+#pragma unroll
+            for (int mm = 1; mm < G; ++mm) v = c == mm ? ld[mm][e] : v;
+            const uint32_t r = k == 0 ? v : __shfl_xor_sync(0xffffffffu, v, k);
+#pragma unroll
+            for (int cc = 0; cc < G; ++cc) pk[8 * cc + e] = c == cc ? r : pk[8 * cc + e];
+        }
+    }
+}
+
 // Eight fp32 values from / to global memory in one 32-byte access (32-byte
 // aligned addresses only).
 __device__ __forceinline__ void ld_global_v8f(const float *p, float *r)
