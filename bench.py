@@ -21,6 +21,7 @@ Prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -74,7 +75,7 @@ def fwd_flops(w):
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, dev_index, uuid=None, period_ms=200):
         self.dev = uuid or str(dev_index)
@@ -94,7 +95,10 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self):
+    def stop(self, windows=None):
+        """Summary of the samples.  windows: {name: [(t0, t1), ...]} in
+        time.time() seconds; adds each window set's median SM clock and mean
+        power (samples whose timestamp falls inside)."""
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -115,9 +119,22 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(power) if power else None}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
+               "reasons": reasons, "samples": len(rows),
+               "power_w_max": max(power) if power else None}
+        for name, spans in (windows or {}).items():
+            inside = []
+            for r in rows:
+                try:
+                    t = datetime.datetime.strptime(r[9], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except (ValueError, IndexError):
+                    continue
+                if any(a <= t <= b for a, b in spans):
+                    inside.append(r)
+            pw = [float(r[3]) for r in inside if r[3].replace(".", "", 1).isdigit()]
+            out[name] = {"sm_mhz": statistics.median(int(r[1]) for r in inside) if inside else None,
+                         "power_w_mean": round(sum(pw) / len(pw), 1) if pw else None, "samples": len(inside)}
+        return out
 
 
 def clocks_rejected(c):
@@ -851,22 +868,27 @@ def main():
     # boxes drops for a while now and then from ~208 GB/s to ~15 GB/s, and a
     # repetition that catches such a drop is copy-bound)
     e2e_all, fwd_only_all = [], []
+    spans = {"fwd_only_phase": [], "e2e_phase": []}   # host wall-clock windows of each phase
     for _ in range(3):
         # the same forward with inputs already in HBM, timed right before the
         # end-to-end steps, so both see the same clocks and power state
+        h0 = time.time()
         t0.record(stream)
         for _ in range(e2e_steps):
             step()
         t1.record(stream)
         torch.cuda.synchronize()
+        spans["fwd_only_phase"].append((h0, time.time()))
         fwd_only_all.append(t0.elapsed_time(t1) / e2e_steps)
+        h0 = time.time()
         t0.record(stream)
         up.wait_event(t0)
         e2e_run(e2e_steps)
         t1.record(stream)
         torch.cuda.synchronize()
+        spans["e2e_phase"].append((h0, time.time()))
         e2e_all.append(t0.elapsed_time(t1) / e2e_steps)
-    e2e_clocks = e2e_sampler.stop()
+    e2e_clocks = e2e_sampler.stop(spans)
     # what the copies do to the forward: one forward with the next step's whole
     # upload running beside it on the copy stream, with the upload and a
     # read-back of the previous outputs beside it (both directions, as in the
@@ -952,6 +974,13 @@ def main():
                 "sm_mhz": e2e_clocks.get("sm_mhz"),
                 "power_w_max": e2e_clocks.get("power_w_max"),
                 "reasons": ",".join(e2e_clocks.get("reasons", [])),
+                # the same samples split by phase (host wall-clock windows): the
+                # copies draw on the board's power budget beside the SMs
+                "sm_mhz_fwd_only_phase": (e2e_clocks.get("fwd_only_phase") or {}).get("sm_mhz"),
+                "sm_mhz_e2e_phase": (e2e_clocks.get("e2e_phase") or {}).get("sm_mhz"),
+                "power_w_fwd_only_phase": (e2e_clocks.get("fwd_only_phase") or {}).get("power_w_mean"),
+                "power_w_e2e_phase": (e2e_clocks.get("e2e_phase") or {}).get("power_w_mean"),
+                "phase_samples": [(e2e_clocks.get(k) or {}).get("samples") for k in ("fwd_only_phase", "e2e_phase")],
                 "note": "pinned host buffers; uploads and read-backs of neighbouring steps "
                         "overlap the forward on two copy streams; fwd_only_ms_per_step is the "
                         "device-only forward timed just before each repetition (same clocks)"},
