@@ -47,12 +47,15 @@ def test_forward_writes_only_its_outputs(cuda_dev, D, shift, S, layout):
         assert bool((head == 77.0).all()) and bool((tail == 77.0).all())
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shift_bytes", [0, 16])
-def test_split_partials_stay_in_the_workspace(cuda_dev, shift_bytes):
+def test_split_partials_stay_in_the_workspace(cuda_dev, shift_bytes, D):
     """The split forward's fp32 partials (32- or 16-byte aligned workspace)
     stay inside ring_attn_fwd_split_workspace bytes; the result is bitwise
-    the same as with a plain workspace."""
-    w = Workload("guard_split", 1, 2, 2, 2048, 128, 4, ZIG, True, torch.bfloat16, seed=131)
+    the same as with a plain workspace (32-byte aligned: the warp regroups its
+    rows so that each store covers whole 128-byte pieces; 16-byte aligned:
+    every lane writes its own row)."""
+    w = Workload("guard_split", 1, 2, 2, 2048, D, 4, ZIG, True, torch.bfloat16, seed=131 + D)
     q, k, v = (t.to(cuda_dev) for t in inputs.make_qkv(w))
     n_split = 3
     ref_out, ref_lse = api.ring_attn_fwd_split(q, k, v, w.N, w.layout, True, n_split=n_split)
@@ -67,13 +70,16 @@ def test_split_partials_stay_in_the_workspace(cuda_dev, shift_bytes):
     assert bool((big[:256 + shift_bytes] == 0xA5).all()) and bool((big[256 + shift_bytes + need:] == 0xA5).all())
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shift", [0, 4])   # fp32 elements: 0 B or 16 B (bf16 out_final: twice as many)
-def test_step_state_stays_in_its_buffers(cuda_dev, shift):
+def test_step_state_stays_in_its_buffers(cuda_dev, shift, D):
     """Two ring steps (flash_block_step) into out_acc / lse_acc / out_final views
     between sentinels, 32- or 16-byte aligned: bitwise the same as plain
-    buffers, and the sentinels untouched."""
+    buffers, and the sentinels untouched.  The plain buffers take the regrouped
+    loads and stores (32-byte aligned), so the 16-byte shift checks them
+    against the per-lane path bit for bit."""
     from context_parallelism_02_gb300 import ring
-    w = Workload("guard_step", 1, 4, 2, 4096, 128, 4, ZIG, True, torch.bfloat16, seed=132)
+    w = Workload("guard_step", 1, 4, 2, 4096, D, 4, ZIG, True, torch.bfloat16, seed=132 + D)
     q, k, v = (t.to(cuda_dev) for t in inputs.make_qkv(w))
     r = 2
     qs = ring.shard(q, r, w.N, w.layout).contiguous()
