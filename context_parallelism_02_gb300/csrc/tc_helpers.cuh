@@ -1,7 +1,9 @@
 // tc_helpers.cuh -- inline-PTX building blocks of the sm_103a tensor-core
 // kernels: shared-memory matrix descriptors, tcgen05 MMA / commit / fences,
-// TMA tile loads with L2 cache hints, MUFU ex2 / lg2, bf16 packing, and the
-// host-side tensor-map encoder for BSHD bf16 tensors.
+// TMA tile loads with L2 cache hints, 32-byte global loads and stores (and the
+// warp-regrouped row loads / stores built on them), MUFU ex2 / lg2, packed fp32
+// arithmetic, bf16 packing, and the host-side tensor-map encoder for BSHD bf16
+// tensors.
 #pragma once
 
 #include <cuda.h>
