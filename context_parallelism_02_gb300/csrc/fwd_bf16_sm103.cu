@@ -12,10 +12,12 @@
 // tile of step N-1.
 //
 // Work unit: one 128-row query tile of one chunk and one (batch, query head),
-// walking 256-key tiles.  S = Q K^T is issued as M=128, N=256 MMAs: on this
-// part an N=128 MMA pays a fixed overhead (about 90 cycles for 64 cycles of
-// work) that an N=256 one hides.  Units are numbered in descending query
-// position, which under a causal mask is descending work.
+// walking 256-key tiles (S = Q K^T as M=128, N=256 MMAs).  Every tile carries a
+// fixed cost beyond its MMAs (about 0.3 us of S read-back, row-max exchange,
+// barrier round trips and MMA completion), so the largest tile that fits the
+// 512 tensor-memory columns beside P and O amortises it best: 192- and 128-key
+// tiles with more buffering of V, S and P measured slower.  Units are numbered
+// in descending query position, which under a causal mask is descending work.
 //
 // Modes (template parameter): the ring over global-order tensors; split-KV
 // partials (a unit's walk cut into pieces, each written in fp32 for a merge
