@@ -113,7 +113,7 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8])
                  : "memory");
 }
 
-// Writes one piece of NW words (NW*4 = 64 or 128 bytes of bf16 pairs) per lane,
+// Writes one piece of NW 32-bit words (64 or 128 bytes: bf16 pairs or fp32) per lane,
 // lane t's piece in its own row (rows anywhere in memory, pieces 32-byte
 // aligned), so that every store instruction covers whole pieces.  A lane storing
 // its own piece would make each instruction touch 32 lines; here lanes in groups
