@@ -34,6 +34,14 @@ def _need_cuda_contig(name, t):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need_out_contig(name, t):
+    # an output may also be pinned host memory, which the kernels address directly
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
 def cp_shard_map(S: int, N: int, layout: int) -> np.ndarray:
     """Global position of each local row, int32 ``[N, S/N]`` (host)."""
     out = np.zeros(S, dtype=np.int32)
@@ -59,8 +67,10 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, N: int, lay
     """Ring / context-parallel attention forward; returns (out, lse).
 
     q ``[B,S,Hq,D]``, k/v ``[B,S,Hkv,D]`` (fp32 or bf16, global order);
-    out like q, lse ``[B,Hq,S]`` fp32.  ``rank_range=(lo, hi)`` restricts the
-    computed queries to virtual ranks [lo, hi) (``ring_attn_fwd_rank``).
+    out like q, lse ``[B,Hq,S]`` fp32.  ``out`` and ``lse`` may be pinned host
+    tensors: the kernels then write the result straight into host memory.
+    ``rank_range=(lo, hi)`` restricts the computed queries to virtual ranks
+    [lo, hi) (``ring_attn_fwd_rank``).
     """
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need_cuda_contig(name, t)
@@ -72,8 +82,8 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, N: int, lay
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-    _need_cuda_contig("out", out)
-    _need_cuda_contig("lse", lse)
+    _need_out_contig("out", out)
+    _need_out_contig("lse", lse)
     sc = -1.0 if scale is None else float(scale)
     L = _lib.load()
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, N, int(causal),

@@ -106,8 +106,12 @@ int cp_schedule_pairs(int64_t S, int N, int layout, int causal, int64_t *pairs_h
  * Fully masked (128-query x 256-key) tile pairs are skipped, so executed
  * work tracks the masked-in work.
  *   q [B][S][Hq][D], k, v [B][S][Hkv][D]: device, dtype CP_F32 or CP_BF16.
- *   out [B][S][Hq][D]: device, same dtype (bf16 rounded to nearest even).
- *   lse [B][Hq][S]: device fp32, lse_i = ln sum_j exp(scale * q_i.k_j).
+ *   out [B][S][Hq][D]: same dtype (bf16 rounded to nearest even).
+ *   lse [B][Hq][S]: fp32, lse_i = ln sum_j exp(scale * q_i.k_j).
+ *   out and lse may be device memory or page-locked host memory that the
+ *   device addresses directly (pinned, unified addressing): the kernels write
+ *   them with ordinary stores, so the result lands in host memory without a
+ *   separate copy.  q, k and v must be device memory.
  *   D in {64, 128}; Hq % Hkv == 0; scale <= 0 selects 1/sqrt(D).
  *   CP_BF16 runs tcgen05 tensor-core kernels (bf16 operands, fp32
  *   accumulation); CP_F32 runs the precision path: fp32 inputs and outputs,

@@ -151,6 +151,27 @@ def test_constant_v(cuda_dev):
     assert (out.float().cpu() - c.float()).abs().max() <= 2 ** -7
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_outputs_in_pinned_host_memory(cuda_dev, dtype):
+    """out and lse given as pinned host tensors: the kernels write the result
+    straight into host memory, bitwise the same as into device buffers (bf16
+    tensor-core path with a persistent and a one-block-per-item launch, and the
+    fp32 path)."""
+    for S, H in ((4096, 2), (8192, 8)) if dtype == torch.bfloat16 else ((512, 2),):
+        w = Workload("host_out", 1, H, H, S, 128 if dtype == torch.bfloat16 else 64, 4, ZIG, True, dtype, seed=27 + S)
+        q, k, v = (t.to(cuda_dev) for t in inputs.make_qkv(w))
+        ref_o, ref_l = api.ring_attn_fwd(q, k, v, w.N, w.layout, True)
+        out_h = torch.full(q.shape, 7.0, dtype=dtype, pin_memory=True)
+        lse_h = torch.full((w.B, w.Hq, w.S), 7.0, dtype=torch.float32, pin_memory=True)
+        o, l = api.ring_attn_fwd(q, k, v, w.N, w.layout, True, out=out_h, lse=lse_h)
+        torch.cuda.synchronize()
+        assert api.cp_get_error() == 0
+        assert o.data_ptr() == out_h.data_ptr() and not o.is_cuda
+        assert torch.equal(out_h, ref_o.cpu()) and torch.equal(lse_h, ref_l.cpu())
+    with pytest.raises(ValueError):
+        api.ring_attn_fwd(q, k, v, w.N, w.layout, True, out=torch.empty(q.shape, dtype=dtype))   # not pinned
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 
