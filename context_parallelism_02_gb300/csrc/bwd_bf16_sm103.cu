@@ -77,6 +77,18 @@ __device__ __forceinline__ void ss_seq(uint32_t tD, uint64_t dA, uint64_t dB, ui
     }
 }
 
+// D/16 MMAs M=128, K=16: A (bf16 pairs, 8 columns per 16 elements) from tensor
+// memory, B K-major in 128-row boxes (16 KB)
+template <int KK, int D>
+__device__ __forceinline__ void ts_k_seq(uint32_t tD, uint32_t tA, uint64_t dB, uint32_t id)
+{
+    if constexpr (KK < D / 16) {
+        constexpr uint32_t ob = (uint32_t)(((KK >> 2) * 16384 + (KK & 3) * 32) >> 4);
+        mma_ts_off<ob>(tD, tA + (uint32_t)(KK * 8), dB, id, KK > 0 ? 1u : 0u);
+        ts_k_seq<KK + 1, D>(tD, tA, dB, id);
+    }
+}
+
 // NK MMAs M=128, N=D, K=16: A (bf16 pairs) from tensor memory, B MN-major
 // (k-steps of 16 rows, 2048 B); A columns relative to tA: 8 KK (MAP 0), or
 // 32 (KK/2) + 8 (KK%2) (MAP 1: two runs of 16 columns, 32 apart).
@@ -135,22 +147,23 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__r
 // ----------------------------------------------------------------------------- dQ
 //
 // Query-stationary.  Tensor memory (columns): S [0,128), dP [128,256), the dQ
-// accumulator [256, 256+D), dS in bf16 pairs [256+D, 320+D).  Shared memory
-// holds the block's Q and dO tiles, three K stages and two V stages: both
-// operands of S = Q K^T and dP = dO V^T come from shared memory, and only
-// dQ += dS K reads its A operand from tensor memory, which the gradient warps
-// load from and store to on every tile.
+// accumulator [256, 256+D), dS in bf16 pairs [256+D, 320+D), the block's dO
+// rows in bf16 pairs [320+D, 320+3D/2).  Shared memory holds the Q tile, four
+// K stages and two V stages.  S = Q K^T reads both operands from shared
+// memory; dP = dO V^T and dQ += dS K read their A operands from tensor memory
+// (dO written there once by the gradient warps, dS on every tile), which
+// halves the shared-memory reads of the dP MMAs.
 //
 // S(j) and dP(j) have their own barriers both ways, so S(j+1) is issued as
 // soon as the gradient warps have read S(j) and runs while they read dP(j)
 // and compute; dQ(j) comes last.  K_j is read by S(j) and by dQ(j); with the
-// MMA order S(j+1), dP(j+1), dQ(j) the load of K(j+3) into the stage of K(j)
-// has two tile groups of MMAs to land.
+// MMA order S(j+1), dP(j+1), dQ(j) the load of K(j+4) into the stage of K(j)
+// has three tile groups of MMAs to land.
 
-constexpr int Q_KST = 3;
+constexpr int Q_KST = 4;
 enum {
     Q_QTM = 0,                   // Q tile landed
-    Q_DOFULL = 1,                // dO tile landed
+    Q_DOFULL = 1,                // dO rows in tensor memory (8 arrivals: the gradient warps)
     Q_KFULL = 2,                 // Q_KST stages
     Q_KEMPTY = 2 + Q_KST,        // Q_KST stages; commits after S(j) and after dQ(j)
     Q_VFULL = 2 + 2 * Q_KST,     // 2 stages
@@ -169,17 +182,16 @@ enum {
 template <int D>
 struct DqCfg {
     static constexpr int TB = Tile<D>::BYTES;
-    static constexpr int OFF_DO = 0;
-    static constexpr int OFF_Q = TB;
-    static constexpr int OFF_K = 2 * TB;                // Q_KST stages
-    static constexpr int OFF_V = (2 + Q_KST) * TB;      // 2 stages
-    static constexpr int OFF_BAR = (4 + Q_KST) * TB;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = TB;                    // Q_KST stages
+    static constexpr int OFF_V = (1 + Q_KST) * TB;      // 2 stages
+    static constexpr int OFF_BAR = (3 + Q_KST) * TB;
     static constexpr int OFF_MISC = OFF_BAR + 8 * Q_NBAR;
     static constexpr int NEED = OFF_MISC + 16;
     static constexpr int SMEM = NEED > 120 * 1024 ? NEED : 120 * 1024;
     static_assert(SMEM <= 232448, "dQ kernel shared memory");
-    static constexpr uint32_t TM_S = 0, TM_P = 128, TM_DQ = 256, TM_DS = 256 + D;
-    static_assert(TM_DS + 64 <= 512, "dQ kernel tensor memory");
+    static constexpr uint32_t TM_S = 0, TM_P = 128, TM_DQ = 256, TM_DS = 256 + D, TM_DO = 320 + D;
+    static_assert(TM_DO + D / 2 <= 512, "dQ kernel tensor memory");
 };
 
 // stage index and phase parity of a ring of NS buffers, advanced once per use
@@ -210,7 +222,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdArgs a, const float *__restrict__ lse,
-                  const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dq)
+                  const float *__restrict__ delta, __nv_bfloat16 *__restrict__ dq,
+                  const __nv_bfloat16 *__restrict__ dout)
 {
     using C = DqCfg<D>;
     constexpr int TB = C::TB;
@@ -220,7 +233,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (threadIdx.x == 0) atomicCAS(a.err, 0u, ERRW_SMEM_ALIGN);
         return;
     }
-    const uint32_t sDO = base + C::OFF_DO, sQ = base + C::OFF_Q, sK = base + C::OFF_K,
+    const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K,
                    sV = base + C::OFF_V, bar0 = base + C::OFF_BAR;
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + C::OFF_MISC);
@@ -236,7 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(Q_QTM), 1);
-        mbar_init(BAR(Q_DOFULL), 1);
+        mbar_init(BAR(Q_DOFULL), 8);
         for (int i = 0; i < Q_KST; ++i) {
             mbar_init(BAR(Q_KFULL + i), 1);
             mbar_init(BAR(Q_KEMPTY + i), 2);
@@ -303,9 +316,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive_expect_tx(BAR(Q_QTM), TB);
             for (int bx = 0; bx < D / 64; ++bx)
                 tma_load5(sQ + bx * 16384, &tmQ, BAR(Q_QTM), bx * 64, w.h, qmr, qmw, w.b, pol_q);
-            mbar_arrive_expect_tx(BAR(Q_DOFULL), TB);
-            for (int bx = 0; bx < D / 64; ++bx)
-                tma_load5(sDO + bx * 16384, &tmDO, BAR(Q_DOFULL), bx * 64, w.h, qmr, qmw, w.b, pol_q);
             KvIter<T> it;
             it.begin(g, w.r, w.qmax);
             int nv = 0;
@@ -323,7 +333,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 volatile int no_abort = 0;
                 WaitCtl dc{a.err, &no_abort, a.drain_ns};
                 wait1(BAR(Q_QTM), 0, dc);
-                wait1(BAR(Q_DOFULL), 0, dc);
                 for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) wait1(BAR(Q_VFULL + (j & 1)), (j >> 1) & 1, dc);
             }
         } else if (warp == 1 || warp == 2) {
@@ -335,11 +344,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint32_t idSP = idesc_bf16(128, T, false);     // K-major A and B
             constexpr uint32_t idDQ = idesc_bf16(128, D, true);      // B = K MN-major
             const uint32_t tS = tmem + C::TM_S, tP = tmem + C::TM_P, tDQ = tmem + C::TM_DQ,
-                           tDS = tmem + C::TM_DS;
+                           tDS = tmem + C::TM_DS, tDO = tmem + C::TM_DO;
             const bool leader = elect_one();
             bool ok = true;
             if (warp == 1) {
-                const uint64_t dDOd = sdesc(sDO, 16, 1024), dQd = sdesc(sQ, 16, 1024);
+                const uint64_t dQd = sdesc(sQ, 16, 1024);
                 const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, 16, 1024);
                 ok = waitw(BAR(Q_QTM), 0, wc) && waitw(BAR(Q_DOFULL), 0, wc);
                 Ring<Q_KST> kr;
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint64_t dV = dV0 + (uint64_t)(sv * (TB >> 4));
                     if (leader) {
                         tc_fence_after();
-                        ss_seq<0, D, 16384>(tP, dDOd, dV, idSP);
+                        ts_k_seq<0, D>(tP, tDO, dV, idSP);   // A = dO from tensor memory
                         mma_commit(BAR(Q_PDONE));
                         mma_commit(BAR(Q_VEMPTY + sv));
                     }
@@ -419,6 +428,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (valid) {
             lse2 = lse[((int64_t)w.b * a.Hq + w.h) * a.S + qp] * LOG2E;
             dlt = delta[((int64_t)w.b * a.Hq + w.h) * a.S + qp];
+        }
+        {
+            // this half's D/2 elements of the row's dO, as D/4 bf16 pairs, into the
+            // A operand of dP = dO V^T (rows past the unit's chunk are zero; their
+            // results are never stored)
+            uint32_t dv4[D / 4];
+            if (valid) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    dout + (((int64_t)w.b * a.S + qp) * a.Hq + w.h) * D + (D / 2) * half);
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    const uint4 x = src[i];
+                    dv4[4 * i] = x.x;
+                    dv4[4 * i + 1] = x.y;
+                    dv4[4 * i + 2] = x.z;
+                    dv4[4 * i + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < D / 4; ++i) dv4[i] = 0u;
+            }
+            const uint32_t tDO = tmem + lane_off + C::TM_DO + (uint32_t)(D / 4) * half;
+            if constexpr (D == 128)
+                tmem_st_x32(tDO, dv4);
+            else
+                tmem_st_x16(tDO, dv4);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_DOFULL));
         }
         bool ok = true;
         KvIter<T> it;
@@ -943,7 +982,7 @@ int launch_bwd_d(const BwdPtrs &p, BwdArgs a, cudaStream_t st)
     if (qunits > 0x7fffffffLL || kunits > 0x7fffffffLL) return CP_EUNSUPPORTED;
     bwd_dq_kernel<D><<<(unsigned)qunits, NTHREADS, DqCfg<D>::SMEM, st>>>(
         mq, mk, mv, mdo, a, p.lse, delta,
-        static_cast<__nv_bfloat16 *>(p.dq));
+        static_cast<__nv_bfloat16 *>(p.dq), static_cast<const __nv_bfloat16 *>(p.dout));
     if (cudaGetLastError() != cudaSuccess) return CP_ECUDA;
     bwd_dkdv_kernel<D><<<(unsigned)kunits, NTHREADS, DkvCfg<D>::SMEM, st>>>(
         mq64, mk, mv, mdo64, a, p.lse, delta, static_cast<__nv_bfloat16 *>(p.dk),
